@@ -1,0 +1,296 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, written without the oracle's own formulas.
+
+Each pin takes an ``oracle.Oracle`` (the real one, or a build with a planted
+mistake) and raises AssertionError when the oracle disagrees with:
+  - hand-worked examples (tests/golden/worked_examples.json);
+  - library routines (scipy softmax / log_softmax, numpy argmax);
+  - the acceptance identity sum_x q(x) P(accept | x) = sum_x min(p(x), q(x))
+    = 1 - TV (page "Optimizing speculative decoding", section "Kimi K3");
+  - target preservation: the emitted token at every position is distributed
+    as the target row, measured exactly on the 2^-24 uniform lattice
+    (same page, section "Rejection sampling and a loss that optimizes
+    acceptance directly", first bullet);
+  - greedy verification = argmax match (same bullet: greedy drafting).
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import scipy.special
+
+import spec_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+LATTICE = 1 << 24
+
+
+def softmax_rows(z, T):
+    z = np.asarray(z, np.float64)
+    if T == 0:
+        out = np.zeros_like(z)
+        idx = np.argmax(z, axis=-1)
+        np.put_along_axis(out, idx[..., None], 1.0, axis=-1)
+        return out
+    return scipy.special.softmax(z / T, axis=-1)
+
+
+def _example_arrays(ex):
+    if "target_probs" in ex:
+        t = np.log(np.array(ex["target_probs"], np.float64)).astype(np.float32)
+        d = np.log(np.array(ex["draft_probs"], np.float64)).astype(np.float32)
+    else:
+        t = np.array(ex["target_logits"], np.float32)
+        d = np.array(ex["draft_logits"], np.float32)
+    return t, d
+
+
+def pin_worked_examples(orc):
+    with open(os.path.join(GOLDEN, "worked_examples.json")) as f:
+        exs = json.load(f)["examples"]
+    for ex in exs:
+        t, d = _example_arrays(ex)
+        k = d.shape[0]
+        r = orc.verify(t[None], d[None], np.array([ex["x"]], np.int32), np.array([ex["T"]], np.float32),
+                       np.array([ex["u"]], np.float32), si.FP32, want_tv=True)
+        assert r["tokens"][0].tolist() == ex["tokens"], (ex["name"], r["tokens"][0])
+        assert int(r["tau"][0]) == ex["tau"], ex["name"]
+        np.testing.assert_allclose(r["p_draft"][0], ex["p_draft"], atol=1e-6, err_msg=ex["name"])
+        np.testing.assert_allclose(r["q_draft"][0], ex["q_draft"], atol=1e-6, err_msg=ex["name"])
+        np.testing.assert_allclose(r["tv"][0], ex["tv"], atol=1e-6, err_msg=ex["name"])
+        assert k == len(ex["x"])
+
+
+def pin_softmax_library(orc):
+    rng = np.random.default_rng(5)
+    for V, T, s in ((16, 1.0, 2.0), (1000, 0.6, 3.0), (4096, 1.7, 0.5), (300, 0.3, 6.0)):
+        z = rng.normal(0, s, V).astype(np.float32)
+        lp, lse = orc.log_softmax(z, T)
+        ref = scipy.special.log_softmax(z.astype(np.float64) / T)
+        np.testing.assert_allclose(lp, ref, rtol=0, atol=1e-12)
+        assert abs(lse - scipy.special.logsumexp(z.astype(np.float64) / T)) < 1e-12
+    # closed form: constant logits c give lse = log V + c / T
+    for V, c, T in ((7, 1.5, 1.0), (151552, -2.25, 0.6)):
+        lp, lse = orc.log_softmax(np.full(V, c, np.float32), T)
+        assert abs(lse - (np.log(V) + c / T)) < 1e-9
+        assert np.allclose(lp, -np.log(V), atol=1e-12)
+    # one dominant logit: p(max) = 1 / (1 + (V-1) e^{-delta/T})
+    V, delta, T = 100, 12.0, 0.8
+    z = np.zeros(V, np.float32)
+    z[37] = delta
+    p = orc.probs(z, T)
+    assert abs(p[37] - 1.0 / (1.0 + (V - 1) * np.exp(-delta / T))) < 1e-14
+    # bf16 rows convert exactly
+    zb = si.f32_to_bf16(rng.normal(0, 2, 64).astype(np.float32))
+    lpb, _ = orc.log_softmax(zb, 1.0, si.BF16)
+    np.testing.assert_allclose(lpb, scipy.special.log_softmax(si.bf16_to_f32(zb).astype(np.float64)), atol=1e-12)
+
+
+def pin_argmax_library(orc):
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        z = rng.integers(-3, 4, 40).astype(np.float32)   # many exact ties
+        assert orc.argmax(z) == int(np.argmax(z))       # numpy returns the first maximum
+    zb = si.f32_to_bf16(np.array([0.5, 2.0, 2.0, 1.0], np.float32))
+    assert orc.argmax(zb, si.BF16) == 1
+
+
+def pin_tv_identities(orc):
+    """TV = 1/2 sum|p - q| = sum max(0, p - q) = 1 - sum min(p, q), from scipy's softmax."""
+    rng = np.random.default_rng(3)
+    B, k, V = 6, 3, 512
+    t = rng.normal(0, 2, (B, k + 1, V)).astype(np.float32)
+    d = (t[:, :k] + rng.normal(0, 0.7, (B, k, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, k)).astype(np.int32)
+    for T in (1.0, float(np.float32(0.6))):   # temperatures enter as fp32
+        r = orc.verify(t, d, x, np.full(B, T, np.float32), np.full((B, k + 1), 0.5, np.float32), si.FP32)
+        p = softmax_rows(t[:, :k], T)
+        q = softmax_rows(d, T)
+        np.testing.assert_allclose(r["tv"], 1.0 - np.minimum(p, q).sum(-1), atol=1e-12)
+        np.testing.assert_allclose(r["tv"], np.maximum(p - q, 0).sum(-1), atol=1e-12)
+        np.testing.assert_allclose(r["p_draft"], np.take_along_axis(p, x[..., None], -1)[..., 0], rtol=1e-12)
+        np.testing.assert_allclose(r["q_draft"], np.take_along_axis(q, x[..., None], -1)[..., 0], rtol=1e-12)
+    # identical rows: TV 0; disjoint one-hots (greedy, different argmax): TV 1
+    r = orc.verify(t, t[:, :k].copy(), x, np.ones(B, np.float32), np.full((B, k + 1), 0.5, np.float32), si.FP32)
+    assert np.all(np.abs(r["tv"]) < 1e-15)
+    d2 = np.zeros_like(d)
+    d2[..., 0] = 100.0
+    t2 = np.zeros_like(t)
+    t2[..., 1] = 100.0
+    r = orc.verify(t2, d2, x, np.zeros(B, np.float32), np.full((B, k + 1), 0.5, np.float32), si.FP32)
+    assert np.all(r["tv"] == 1.0)
+
+
+def lattice_boundary(pred, n_queries: int) -> np.ndarray:
+    """For monotone predicates (True below a threshold N*, False from N* on) over
+    n in [0, 2^24], return N* per query by bisection.  pred(ns) -> bool array."""
+    lo = np.zeros(n_queries, np.int64)          # pred(lo) True or lo == 0
+    hi = np.full(n_queries, LATTICE, np.int64)  # first n with pred False is <= hi
+    while True:
+        active = hi > lo
+        if not active.any():
+            return lo
+        mid = (lo + hi) // 2
+        ok = pred(mid)
+        lo = np.where(active & ok, mid + 1, lo)
+        hi = np.where(active & ~ok, mid, hi)
+
+
+def acceptance_masses(orc, lp, lq):
+    """Exact lattice measure of {u : oracle accepts} for arrays of (log p, log q)."""
+    lp = np.asarray(lp, np.float64).ravel()
+    lq = np.asarray(lq, np.float64).ravel()
+
+    def pred(ns):
+        return np.array([orc.accept(a, b, n / LATTICE)[0] for a, b, n in zip(lp, lq, ns)])
+    return lattice_boundary(pred, lp.size) / LATTICE
+
+
+def pin_acceptance_is_overlap(orc):
+    """sum_x q(x) P(accept | x) = sum_x min(p, q) = 1 - TV (exact, on the lattice)."""
+    rng = np.random.default_rng(13)
+    V = 12
+    for T in (1.0, float(np.float32(0.7))):
+        zt = rng.normal(0, 2, V).astype(np.float32)
+        zd = (zt + rng.normal(0, 0.8, V)).astype(np.float32)
+        p = softmax_rows(zt, T)
+        q = softmax_rows(zd, T)
+        lp, _ = orc.log_softmax(zt, T)
+        lq, _ = orc.log_softmax(zd, T)
+        A = acceptance_masses(orc, lp, lq)
+        # lattice measure is within one lattice step of min(1, p/q)
+        np.testing.assert_allclose(A, np.minimum(1.0, p / q), atol=1.0 / LATTICE + 1e-12)
+        assert abs((q * A).sum() - np.minimum(p, q).sum()) < 2.0 / LATTICE
+        assert abs((q * A).sum() - (1.0 - 0.5 * np.abs(p - q).sum())) < 2.0 / LATTICE
+
+
+def _tiny_rows(seed=0, T=1.0):
+    w = si.TINY if seed == 0 else si.TINY.scaled(seed=seed)
+    b = si.generate(w)
+    return b.target[0], b.draft[0], w
+
+
+def pin_target_preservation_exact(orc, seed=0):
+    """Exact output distribution of the chain driver on the tiny workload
+    (V = 16, k = 3): for every draft tuple x (16^3, weight prod q_i(x_i)), the
+    accept decisions and the final draw are measured on the 2^-24 uniform
+    lattice by bisection over the oracle's own verify call.  Then
+        P(y_j = a, n >= j) = p_j(a) * prod_{i<j} (1 - TV_i)   for j = 1..k+1
+    (the emitted token at each position follows the target; n = tau + 1)."""
+    t, d, w = _tiny_rows(seed)
+    k, V, T = w.k, w.vocab, 1.0
+    p = softmax_rows(t, T)          # [k+1, V]
+    q = softmax_rows(d, T)          # [k, V]
+    tv = 0.5 * np.abs(p[:k] - q).sum(-1)
+
+    tuples = np.stack(np.meshgrid(*[np.arange(V)] * k, indexing="ij"), -1).reshape(-1, k).astype(np.int32)
+    nT = tuples.shape[0]
+
+    def run(x, u):
+        n = x.shape[0]
+        return orc.verify(np.broadcast_to(t, (n,) + t.shape), np.broadcast_to(d, (n,) + d.shape), x,
+                          np.full(n, T, np.float32), u, si.FP32, want_tv=False, nthreads=8)
+
+    # A[tuple, i]: lattice measure of acceptance at position i, earlier positions
+    # accepted with u = 0 (p > 0 everywhere at T = 1), later uniforms arbitrary.
+    A = np.zeros((nT, k))
+    for i in range(k):
+        def pred(ns, i=i):
+            u = np.zeros((nT, k + 1), np.float32)
+            u[:, i] = ns / LATTICE
+            return run(tuples, u)["tau"] > i
+        A[:, i] = lattice_boundary(pred, nT) / LATTICE
+
+    # R[i, xi, a]: final-token distribution after a rejection at position i
+    # with rejected draft xi (only where a rejection is possible: p_i(xi) < q_i(xi)).
+    # Bonus[a]: final-token distribution when every draft is accepted.
+    def final_token_dist(x_rows, u_fixed, pos):
+        n = x_rows.shape[0]
+        bounds = np.zeros((n, V + 1), np.int64)
+        bounds[:, V] = LATTICE
+        for a in range(1, V):
+            def pred(ns, a=a):
+                u = u_fixed.copy()
+                u[:, k] = ns / LATTICE
+                return run(x_rows, u)["tokens"][np.arange(n), pos] < a
+            bounds[:, a] = lattice_boundary(pred, n)
+        return np.diff(bounds, axis=1) / LATTICE
+
+    R = np.zeros((k, V, V))
+    for i in range(k):
+        rej = np.nonzero(p[i] < q[i])[0]
+        if rej.size == 0:
+            continue
+        x_rows = np.zeros((rej.size, k), np.int32)
+        x_rows[:, i] = rej
+        u_fixed = np.zeros((rej.size, k + 1), np.float32)
+        u_fixed[:, i] = (LATTICE - 1) / LATTICE          # reject at i (p/q < 1 - 2^-24 there)
+        assert np.all(run(x_rows, u_fixed)["tau"] == i)
+        R[i, rej] = final_token_dist(x_rows, u_fixed, i)
+    bonus = final_token_dist(np.zeros((1, k), np.int32), np.zeros((1, k + 1), np.float32), k)[0]
+
+    wq = np.prod(q[np.arange(k), tuples], axis=1)       # weight of each tuple
+    reach = np.ones(nT)
+    for j in range(k):
+        xj = tuples[:, j]
+        emit = np.zeros((nT, V))
+        emit[np.arange(nT), xj] += A[:, j]
+        emit += (1.0 - A[:, j])[:, None] * R[j, xj]
+        got = (wq[:, None] * reach[:, None] * emit).sum(0)
+        want = p[j] * np.prod(1.0 - tv[:j])
+        np.testing.assert_allclose(got, want, atol=4e-6, err_msg=f"position {j + 1}")
+        # P(n = j+1) = prod_{i<j}(1 - TV_i) * TV_j
+        p_stop = (wq * reach * (1.0 - A[:, j])).sum()
+        assert abs(p_stop - np.prod(1.0 - tv[:j]) * tv[j]) < 4e-6
+        reach = reach * A[:, j]
+    got = (wq * reach).sum() * bonus
+    np.testing.assert_allclose(got, p[k] * np.prod(1.0 - tv), atol=4e-6, err_msg="bonus position")
+
+
+def pin_greedy_is_argmax_match(orc):
+    rng = np.random.default_rng(21)
+    B, k, V = 40, 5, 64
+    t = rng.integers(-4, 5, (B, k + 1, V)).astype(np.float32)   # frequent ties
+    d = rng.integers(-4, 5, (B, k, V)).astype(np.float32)
+    am_t = np.argmax(t, -1)
+    am_d = np.argmax(d, -1)
+    # drafts: the draft argmax, except that some chains copy the target argmax
+    x = am_d.copy()
+    copy = rng.random((B, k)) < 0.7
+    x[copy] = am_t[:, :k][copy]
+    x = x.astype(np.int32)
+    r = orc.verify(t, d, x, np.zeros(B, np.float32), rng.random((B, k + 1)).astype(np.float32), si.FP32)
+    match = x == am_t[:, :k]
+    tau = np.where(match.all(1), k, np.argmin(match, 1))
+    assert np.array_equal(r["tau"], tau)
+    for b in range(B):
+        assert r["tokens"][b, :tau[b]].tolist() == x[b, :tau[b]].tolist()
+        assert r["tokens"][b, tau[b]] == am_t[b, tau[b]]
+        assert np.all(r["tokens"][b, tau[b] + 1:] == -1)
+    assert np.array_equal(r["tv"], (am_t[:, :k] != am_d).astype(np.float64))
+
+
+def pin_inverse_cdf_library(orc):
+    """Final draw = first index whose inclusive cumulative weight exceeds u*S
+    (numpy searchsorted, side='right'); zero-weight tokens are never drawn."""
+    rng = np.random.default_rng(17)
+    for _ in range(200):
+        V = int(rng.integers(1, 40))
+        w = rng.random(V) * (rng.random(V) < 0.6)
+        if w.sum() == 0:
+            w[rng.integers(V)] = 0.5
+        u = float(rng.integers(0, LATTICE)) / LATTICE
+        y, _, S = orc.sample(w, u)
+        c = np.cumsum(w)
+        assert abs(S - c[-1]) < 1e-12
+        assert y == int(np.searchsorted(c, u * c[-1], side="right")), (w, u, y)
+        assert w[y] > 0
+    w = np.array([0.0, 0.25, 0.0, 0.5, 0.25])
+    assert orc.sample(w, 0.25)[0] == 3        # exactly on C_1: strict inequality moves past it
+    assert orc.sample(w, 0.0)[0] == 1         # the first positive weight, not index 0
+
+
+ALL_PINS = [pin_worked_examples, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
+            pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact]
