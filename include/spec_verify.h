@@ -1,0 +1,162 @@
+/*
+ * spec_verify: batched speculative-decoding verification by rejection
+ * sampling, for one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (per chain b of k drafted tokens x_1..x_k):
+ *   p_i = softmax(target_logits[b, i-1, :] / T_b)   i = 1..k+1   (target rows)
+ *   q_i = softmax(draft_logits[b, i-1, :] / T_b)    i = 1..k     (draft rows)
+ *   Drafts are accepted or rejected against the target distribution, which
+ *   preserves it ("Optimizing speculative decoding", section "Rejection
+ *   sampling and a loss that optimizes acceptance directly", first bullet):
+ *   x_i is accepted while u_i < min(1, p_i(x_i) / q_i(x_i)).  At the first
+ *   rejection (position tau+1) one token is drawn from the normalised residual
+ *   max(0, p - q); if all k are accepted, a bonus token is drawn from p_{k+1}
+ *   (the k+1-th target row that the single verification pass provides:
+ *   same page, "The draft model moved inside").  The final draw uses its own
+ *   uniform u_{k+1} and the inverse CDF y = min{ j : u * S < C_j }.
+ *   tau is the accepted length (page "DSpark for GLM-5.2", introduction).
+ *   The per-position total-variation distance 0.5 * sum_j |p_i(j) - q_i(j)|
+ *   (first page, same section, second bullet) is reported for every
+ *   position; 1 - TV is the per-position acceptance probability
+ *   sum_j min(p, q) (first page, section "Kimi K3").
+ *   T_b == 0 means greedy: p and q are one-hot on the lowest-index maximum,
+ *   so a draft is accepted iff it equals the target argmax.
+ *
+ * Conventions shared by every entry point:
+ *   - Logit tensors are dense, row-major, C-contiguous, in device memory,
+ *     element type fp32 (SV_FP32) or bf16 (SV_BF16).  A logit row must
+ *     contain no NaN and no +inf; -inf marks a masked token; at least one
+ *     entry must be finite; for T > 0, |max logit| / T must stay below
+ *     2^22 / log2(e).  A chain that breaks any of these, has a temperature
+ *     that is negative, NaN or infinite, or a draft token outside [0, V), is
+ *     an invalid chain: its tau is -1 and its tokens are -1 (no fault).
+ *   - All pointers are device pointers unless the name says host; the caller
+ *     owns every buffer; the library only reads inputs and writes outputs.
+ *   - Calls are asynchronous and ordered on the caller's CUDA stream
+ *     (`cuda_stream` is a cudaStream_t; NULL = the legacy default stream).
+ *     Nothing is returned to the host until the caller synchronises, except
+ *     by spec_verify_get_error, which synchronises.
+ *   - Argument errors are detected on the host before any launch and
+ *     returned as a status; no exception crosses the interface.
+ *   - A handle is not thread-safe; use one handle per stream.
+ *   - Uniforms are in [0, 1); the seeded generator used by this project
+ *     produces them on the 2^-24 lattice.
+ *   - Limits: 1 <= k <= 31; V <= 163840 (bf16) or 81920 (fp32).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_verify_ctx* spec_verify_t;
+
+/* Status codes returned by every call. */
+enum {
+  SV_OK = 0,
+  SV_ERR_ARG = 1,     /* null handle/pointer, bad batch size, misaligned array */
+  SV_ERR_DTYPE = 2,   /* unknown logit dtype */
+  SV_ERR_SIZE = 3,    /* k or V outside the supported range */
+  SV_ERR_CUDA = 4,    /* a CUDA runtime call or launch failed */
+  SV_ERR_ALLOC = 5,   /* device or host allocation failed in init */
+  SV_ERR_DATA = 6,    /* (get_error) some chains were invalid since the last check */
+  SV_ERR_TIMEOUT = 7  /* (get_error) a bounded device wait expired; outputs of that call are unreliable */
+};
+
+/* Logit element types. */
+enum { SV_FP32 = 0, SV_BF16 = 1 };
+
+/* Flags for spec_verify_init. */
+enum {
+  SV_FLAG_HOST_STAGING = 1u,  /* also allocate device staging for spec_verify_host */
+  SV_FLAG_NO_TMA = 2u,        /* load logits with plain loads instead of bulk copies (testing) */
+  SV_FLAG_KERNEL_TIMING = 4u  /* record a CUDA event pair around the verification kernel of each call */
+};
+
+/* Create a handle for chains of k drafts over a vocabulary of `vocab`
+ * tokens with logits of type `logit_dtype`, for batches of up to
+ * `max_batch` chains.  Allocates the device workspace (per-position accept
+ * decisions, candidate tokens and status words: about 9*(k+1) bytes per
+ * chain) and, with SV_FLAG_HOST_STAGING, device copies of every input and
+ * output for max_batch chains.  Uses the current CUDA device; the handle
+ * must be used on that device.  Writes NULL to *h on failure. */
+int spec_verify_init(spec_verify_t* h, int max_batch, int k, int vocab, int logit_dtype, unsigned flags);
+
+/* Verify `batch` chains (0 <= batch <= max_batch).
+ *   target_logits  [batch, k+1, V]  row i is the target distribution after x_1..x_i
+ *   draft_logits   [batch, k,   V]  row i is the distribution x_{i+1} was drawn from
+ *   draft_tokens   [batch, k]   int32
+ *   temperature    [batch]      fp32, one per chain, 0 = greedy
+ *   uniforms       [batch, k+1] fp32 in [0,1): u[:, 0..k-1] accept tests,
+ *                               u[:, k] the final (residual or bonus) draw
+ *   out_tokens     [batch, k+1] int32: x_1..x_tau, then the residual or bonus
+ *                               token, then -1 padding
+ *   out_tau        [batch]      int32: accepted drafts 0..k (-1: invalid chain)
+ *   out_p_draft    [batch, k]   fp32 or NULL: p_i(x_i) for every position
+ *   out_q_draft    [batch, k]   fp32 or NULL: q_i(x_i) for every position
+ *   out_tv         [batch, k]   fp32 or NULL: TV distance of every position
+ * Integer and fp32 arrays must be 4-byte aligned; logits whose base is
+ * 16-byte aligned and whose row size V*sizeof(elem) is a multiple of 16 use
+ * bulk (TMA) copies, anything else plain loads.  Two kernel launches. */
+int spec_verify(spec_verify_t h, int batch,
+                const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                int32_t* out_tokens, int32_t* out_tau,
+                float* out_p_draft, float* out_q_draft, float* out_tv,
+                void* cuda_stream);
+
+/* Per-position TV distance only: out_tv[b, i] = 0.5 * sum_j |p_{i+1}(j) - q_{i+1}(j)|
+ * for the k target/draft row pairs of each chain (the target's bonus row is
+ * not read).  An invalid chain gets NaN.  One kernel launch. */
+int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                   const float* temperature, float* out_tv, void* cuda_stream);
+
+/* spec_verify for callers whose inputs and outputs live in host memory
+ * (pinned memory gives the fastest copies).  Same arguments and layouts as
+ * spec_verify, but every pointer is a host pointer; the handle must have been
+ * created with SV_FLAG_HOST_STAGING.  Copies inputs to the handle's device
+ * staging, verifies, copies outputs back, all on `cuda_stream`; the call
+ * returns after enqueueing (synchronise the stream before reading outputs). */
+int spec_verify_host(spec_verify_t h, int batch,
+                     const void* host_target_logits, const void* host_draft_logits,
+                     const int32_t* host_draft_tokens, const float* host_temperature,
+                     const float* host_uniforms,
+                     int32_t* host_out_tokens, int32_t* host_out_tau,
+                     float* host_out_p_draft, float* host_out_q_draft, float* host_out_tv,
+                     void* cuda_stream);
+
+/* Synchronise the device and report what the kernels flagged since the last
+ * call: SV_OK, SV_ERR_DATA (with the number of invalid chains, or invalid
+ * positions for spec_verify_tv, in *invalid_count if non-NULL),
+ * SV_ERR_TIMEOUT, or SV_ERR_CUDA.  Clears the flags. */
+int spec_verify_get_error(spec_verify_t h, int* invalid_count);
+
+/* Launch geometry chosen at init: vocabulary slices per row (thread-block
+ * cluster size), persistent clusters, register rounds per thread, whether
+ * bulk copies are enabled, and kernel launches per spec_verify call.
+ * Any pointer may be NULL. */
+int spec_verify_info(spec_verify_t h, int* cluster_size, int* n_clusters, int* rounds, int* tma,
+                     int* launches_per_call);
+
+/* With SV_FLAG_KERNEL_TIMING: wait for the recorded events and write the
+ * duration in milliseconds of the verification kernel (the first of the
+ * two launches of spec_verify, or the only launch of spec_verify_tv) of up
+ * to max_n calls made since the previous read into out_ms, oldest first;
+ * *n_out receives the count.  At most 4096 calls are recorded between reads.
+ * Returns SV_ERR_ARG if the handle was created without the flag. */
+int spec_verify_kernel_times(spec_verify_t h, float* out_ms, int max_n, int* n_out);
+
+/* Free the handle and its device memory (NULL is a no-op). */
+void spec_verify_destroy(spec_verify_t h);
+
+/* Static description of a status code. */
+const char* spec_verify_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

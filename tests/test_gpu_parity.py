@@ -1,0 +1,191 @@
+"""CUDA library (through the C ABI) against the CPU oracle, on the same seeded inputs."""
+import numpy as np
+import pytest
+
+import spec_inputs as si
+from tests import _parity
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_68_gb300 as sv
+    sv.build()
+    return sv
+
+
+def to_dev(b: si.Batch):
+    dev = torch.device("cuda")
+    if b.workload.dtype == si.BF16:
+        tgt = torch.from_numpy(b.target.view(np.int16)).to(dev).view(torch.bfloat16)
+        dft = torch.from_numpy(b.draft.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        tgt = torch.from_numpy(b.target).to(dev)
+        dft = torch.from_numpy(b.draft).to(dev)
+    return (tgt, dft, torch.from_numpy(b.tokens).to(dev), torch.from_numpy(b.temperature).to(dev),
+            torch.from_numpy(b.uniforms).to(dev))
+
+
+def run_gpu(lib, w, b, flags=0, want_tv=True):
+    v = lib.SpecVerifier(max(1, b.nb), w.k, w.vocab, torch.float32 if w.dtype == si.FP32 else torch.bfloat16, flags)
+    out = v.verify(*to_dev(b), want_tv=want_tv)
+    torch.cuda.synchronize()
+    res = {k: t.cpu().numpy() for k, t in out.items()}
+    rc, n_bad = v.get_error()
+    v.close()
+    return res, rc, n_bad
+
+
+def check(lib, oracle, w, b=None, flags=0):
+    b = b if b is not None else si.generate(w)
+    got, rc, n_bad = run_gpu(lib, w, b, flags)
+    ref = oracle.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, nthreads=16)
+    stats = _parity.assert_parity(got, ref, w.k)
+    n_invalid = int((ref["tau"] < 0).sum())
+    assert n_bad == n_invalid and (rc == 0) == (n_invalid == 0), (rc, n_bad, n_invalid)
+    print(w.name, stats)
+    return got, ref, stats
+
+
+# -------- the five workloads at full size (every chain compared)
+@pytest.mark.parametrize("w", [si.TINY, si.C2, si.C3_T0, si.C3_T06, si.C3_T1, si.C4, si.C5], ids=lambda w: w.name)
+def test_workload_full(lib, oracle, w):
+    check(lib, oracle, w)
+
+
+# -------- smaller cases spanning tiles and ragged tails
+@pytest.mark.parametrize("V,dtype", [(16, si.FP32), (37, si.FP32), (1000, si.FP32), (1001, si.FP32), (4096, si.BF16),
+                                     (2050, si.BF16), (20000, si.BF16), (32001, si.BF16), (81920, si.FP32),
+                                     (163840, si.BF16)])
+@pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
+def test_ragged_vocab(lib, oracle, V, dtype, T):
+    w = si.Workload(f"ragged_V{V}", 6, 5, V, dtype, 2.0, draft_sigma=0.8, temp_lo=T, temp_hi=T)
+    check(lib, oracle, w)
+
+
+@pytest.mark.parametrize("k", [1, 2, 15, 31])
+def test_draft_lengths(lib, oracle, k):
+    w = si.Workload(f"k{k}", 5, k, 3000, si.BF16, 1.0, draft_sigma=0.3, temp_mode=1, temp_lo=0.5, temp_hi=1.5)
+    check(lib, oracle, w)
+
+
+def test_no_tma_path_bit_identical(lib):
+    w = si.C3_T06.scaled(batch=6)
+    b = si.generate(w)
+    a, _, _ = run_gpu(lib, w, b)
+    c, _, _ = run_gpu(lib, w, b, flags=lib.SV_FLAG_NO_TMA)
+    for key in a:
+        assert np.array_equal(a[key], c[key]), key
+
+
+def test_deterministic(lib):
+    w = si.C4.scaled(batch=16)
+    b = si.generate(w)
+    a, _, _ = run_gpu(lib, w, b)
+    c, _, _ = run_gpu(lib, w, b)
+    for key in a:
+        assert np.array_equal(a[key], c[key], equal_nan=True), key
+
+
+def test_identical_rows_accept_all(lib, oracle):
+    w = si.C3_T06.scaled(batch=8, vocab=151552)
+    b = si.generate(w)
+    b.draft[:] = b.target[:, :w.k]
+    got, ref, _ = check(lib, oracle, w, b)
+    assert np.all(got["tau"] == w.k) and np.all(got["tv"] == 0.0)
+
+
+def test_greedy_ties_lowest_index(lib, oracle):
+    rng = np.random.default_rng(4)
+    w = si.Workload("greedy_ties", 32, 7, 5000, si.FP32, 1.0, temp_lo=0.0, temp_hi=0.0)
+    b = si.generate(w)
+    b.target[:] = rng.integers(-3, 4, b.target.shape).astype(np.float32)
+    b.draft[:] = rng.integers(-3, 4, b.draft.shape).astype(np.float32)
+    am = np.argmax(b.target, -1)
+    b.tokens[:] = np.where(rng.random((32, 7)) < 0.8, am[:, :7], np.argmax(b.draft, -1)).astype(np.int32)
+    check(lib, oracle, w, b)
+
+
+def test_invalid_chains_flagged(lib, oracle):
+    w = si.C2.scaled(batch=8, vocab=2048)
+    b = si.generate(w)
+    b.tokens[1, 3] = w.vocab          # out of range
+    b.tokens[2, 0] = -5
+    b.temperature[3] = -1.0
+    b.temperature[4] = np.nan
+    b.target[5, 7, 11] = np.nan       # bonus row
+    b.draft[6, 2, :] = -np.inf        # no finite logit
+    b.draft[7, 2, 5] = -np.inf        # a masked token: still valid
+    got, ref, _ = check(lib, oracle, w, b)
+    assert list(np.nonzero(got["tau"] < 0)[0]) == [1, 2, 3, 4, 5, 6]
+
+
+def test_spec_verify_tv(lib, oracle):
+    w = si.C5.scaled(batch=24)
+    b = si.generate(w)
+    v = lib.SpecVerifier(24, w.k, w.vocab, torch.bfloat16)
+    tgt, dft, _, tmp, _ = to_dev(b)
+    tv = v.verify_tv(tgt, dft, tmp).cpu().numpy()
+    ref = oracle.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, nthreads=16)
+    err = np.abs(tv - ref["tv"])
+    assert np.all(err <= _parity.TV_RTOL * ref["tv"] + _parity.TV_ATOL)
+    v.close()
+
+
+def test_host_entry_point(lib):
+    w = si.C3_T1.scaled(batch=8)
+    b = si.generate(w)
+    dev, _, _ = run_gpu(lib, w, b)
+    v = lib.SpecVerifier(8, w.k, w.vocab, torch.bfloat16, flags=lib.SV_FLAG_HOST_STAGING)
+    tg = torch.from_numpy(b.target.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dr = torch.from_numpy(b.draft.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_out = v.alloc_outputs(8, want_pq=True, want_tv=True, device="cpu")
+    host_out = {k: t.pin_memory() for k, t in host_out.items()}
+    v.verify_host(tg, dr, torch.from_numpy(b.tokens), torch.from_numpy(b.temperature), torch.from_numpy(b.uniforms),
+                  host_out)
+    torch.cuda.synchronize()
+    for key in dev:
+        assert np.array_equal(dev[key], host_out[key].numpy()), key
+    v.close()
+
+
+def test_empty_batch_and_bad_args(lib):
+    v = lib.SpecVerifier(4, 3, 64, torch.float32)
+    e = torch.empty((0, 4, 64), device="cuda")
+    out = v.verify(e, torch.empty((0, 3, 64), device="cuda"), torch.empty((0, 3), dtype=torch.int32, device="cuda"),
+                   torch.empty((0,), device="cuda"), torch.empty((0, 4), device="cuda"))
+    assert out["tokens"].shape == (0, 4)
+    with pytest.raises(lib.SpecVerifyError):
+        lib.SpecVerifier(4, 32, 64, torch.float32)     # k above the limit
+    with pytest.raises(lib.SpecVerifyError):
+        lib.SpecVerifier(4, 7, 200000, torch.bfloat16)  # V above the limit
+    v.close()
+
+
+def test_target_preservation_sampled_gpu(lib, oracle):
+    """The GPU passes the same chi-squared test as the oracle (tiny rows, 200,000 chains)."""
+    import scipy.stats
+    from tests import _pins
+    n = 200_000
+    base = si.generate(si.TINY)
+    k, V = si.TINY.k, si.TINY.vocab
+    t = np.ascontiguousarray(np.broadcast_to(base.target[0], (n, k + 1, V)))
+    d = np.ascontiguousarray(np.broadcast_to(base.draft[0], (n, k, V)))
+    x = si.gumbel_argmax(303, d, si.FP32, np.ones(n * k, np.float32)).astype(np.int32)
+    u = si.uniforms(303, si.STREAM_VERIFY, 0, n, k + 1)
+    b = si.Batch(si.TINY.scaled(batch=n), 0, t, d, x, np.ones(n, np.float32), u)
+    got, _, _ = run_gpu(lib, b.workload, b)
+    ref = oracle.verify(t, d, x, np.ones(n, np.float32), u, si.FP32, nthreads=16)
+    _parity.assert_parity(got, ref, k)
+    p = _pins.softmax_rows(t[0], 1.0)
+    emitted = got["tau"] + 1
+    for j in range(k + 1):
+        sel = emitted >= j + 1
+        counts = np.bincount(got["tokens"][sel, j], minlength=V)
+        exp = p[j] * sel.sum()
+        keep = exp > 5
+        assert scipy.stats.chisquare(counts[keep], exp[keep] * counts[keep].sum() / exp[keep].sum()).pvalue > 1e-4
