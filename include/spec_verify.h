@@ -79,9 +79,9 @@ enum {
 /* Create a handle for chains of k drafts over a vocabulary of `vocab`
  * tokens with logits of type `logit_dtype`, for batches of up to
  * `max_batch` chains.  Allocates the device workspace (per-position accept
- * decisions, candidate tokens and status words: about 9*(k+1) bytes per
- * chain) and, with SV_FLAG_HOST_STAGING, device copies of every input and
- * output for max_batch chains.  Uses the current CUDA device; the handle
+ * decisions, greedy tokens, row statistics and per-range masses: about
+ * 552*(k+1) bytes per chain) and, with SV_FLAG_HOST_STAGING, device copies of
+ * every input and output for max_batch chains.  Uses the current CUDA device; the handle
  * must be used on that device.  Writes NULL to *h on failure. */
 int spec_verify_init(spec_verify_t* h, int max_batch, int k, int vocab, int logit_dtype, unsigned flags);
 
@@ -110,7 +110,8 @@ int spec_verify(spec_verify_t h, int batch,
 
 /* Per-position TV distance only: out_tv[b, i] = 0.5 * sum_j |p_{i+1}(j) - q_{i+1}(j)|
  * for the k target/draft row pairs of each chain (the target's bonus row is
- * not read).  An invalid chain gets NaN.  One kernel launch. */
+ * not read).  A position whose rows or temperature are invalid gets NaN.
+ * Two kernel launches. */
 int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
                    const float* temperature, float* out_tv, void* cuda_stream);
 
@@ -129,9 +130,9 @@ int spec_verify_host(spec_verify_t h, int batch,
                      void* cuda_stream);
 
 /* Synchronise the device and report what the kernels flagged since the last
- * call: SV_OK, SV_ERR_DATA (with the number of invalid chains, or invalid
- * positions for spec_verify_tv, in *invalid_count if non-NULL),
- * SV_ERR_TIMEOUT, or SV_ERR_CUDA.  Clears the flags. */
+ * call: SV_OK, SV_ERR_DATA (with the number of invalid chains in
+ * *invalid_count if non-NULL), SV_ERR_TIMEOUT, or SV_ERR_CUDA.  Clears the
+ * flags. */
 int spec_verify_get_error(spec_verify_t h, int* invalid_count);
 
 /* Launch geometry chosen at init: vocabulary slices per row (thread-block

@@ -2,32 +2,32 @@
 // on one GB300 (sm_103a).  The C interface and the method are described in
 // include/spec_verify.h; this file holds the kernels and the host side.
 //
-// Design (one pass over HBM):
+// Design (every logit row is streamed from HBM once):
 //   * A "unit" is one position of one chain: the pair (target row i, draft
 //     row i) for i < k, or the single bonus target row k.  Every unit is
 //     processed by one thread-block cluster of C CTAs (C <= 8); CTA r owns the
-//     vocabulary slice [r*Vs, (r+1)*Vs) of both rows.
+//     vocabulary slice [r*Vs, (r+1)*Vs) of both rows, and warp w of the CTA a
+//     contiguous range of WV 16-byte vectors of that slice.
 //   * The kernel is persistent: each cluster walks units cluster_id,
 //     cluster_id + n_clusters, ...  Two CTAs share an SM.  Each CTA has one
 //     shared-memory stage; a bulk (TMA) copy lands the next unit's slice there
-//     while the current unit is processed from registers.
+//     while the current unit is processed from registers.  The last warp to
+//     copy its part out of the stage issues the next copy.
 //   * Pass A (registers): per-row maximum, then sum of exp2(z*c - R) with an
 //     integer reference R = ceil(max*c), c = log2(e)/T.  Integer references
 //     make every rescale between warps and CTAs an exact power of two.
-//   * Exchange 1 (DSMEM push + cluster barrier): per-CTA (max, sum) of both
-//     rows; every CTA merges the same values in the same order.
+//   * Exchange (DSMEM push + one cluster barrier per unit): every warp pushes
+//     its (max, sum) of both rows to every CTA; each warp merges the C*8
+//     parts in the same order, so all CTAs hold identical row statistics.
 //   * Pass B (registers): with e_j = 2^(z_j*c - R) and r = S_t/S_d, the
-//     weight w_j = max(0, e_t - r*e_d) = S_t * max(0, p_j - q_j) (one rounding,
-//     exactly zero for identical rows); per-thread, per-round partial sums.
-//     The CTA owning the drafted token evaluates the accept test.
-//   * Exchange 2: per-CTA residual mass W_c and the accept decision.  The sum
-//     of W_c divided by S_t is the TV distance.  If the draft was rejected (or the unit is
-//     the bonus row) the CTA whose slice contains u*S draws the token by a
-//     hierarchical inverse-CDF search (round/warp table, lane scan, element).
-//     The draw is made for every rejected position, so no second pass over
-//     HBM is needed once tau is known.
-//   * A small finalize kernel (one warp per chain) finds the first rejection
-//     with a ballot and writes tokens and tau.
+//     residual weight w_j = max(0, e_t - r*e_d) = S_t * max(0, p_j - q_j) (one
+//     rounding, exactly zero for identical rows).  Each warp writes the sum of
+//     w over its range (and its share of sum e_t) to a small workspace; the
+//     CTA owning the drafted token evaluates the accept test.
+//   * A finalize kernel (one warp per chain) finds the first rejection tau
+//     with a ballot, adds the per-warp masses into the TV distances, locates
+//     the warp range holding u * (total mass) of unit tau, re-reads that one
+//     range (1/(8C) of the rows) and finishes the inverse-CDF draw.
 //   Greedy chains (T == 0) use only the maximum and its lowest index.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -43,13 +43,26 @@ namespace {
 constexpr int NT = 256;            // threads per CTA
 constexpr int NWARP = NT / 32;
 constexpr int CMAX = 8;            // largest cluster
-constexpr int SMALL_BYTES = 6144;  // bookkeeping area in front of the stage
+constexpr int ITEMS_MAX = CMAX * NWARP;
+constexpr int SMALL_BYTES = 4352;  // bookkeeping area in front of the stage
 constexpr float LOG2E_F = 1.44269504088896341f;
 constexpr float REF_LIMIT = 4194304.0f;   // |max * c| must stay below 2^22
 constexpr unsigned FULL = 0xffffffffu;
 
 // status bits of a unit
 constexpr int ST_TEMP = 1, ST_TOKEN = 2, ST_ROW = 4;
+
+// Per-unit statistics kept for the finalize kernel.
+struct alignas(16) UnitStat {
+  float c;       // log2(e) / T, 0 for greedy units
+  float R_t;     // integer references of the target / draft row
+  float R_d;
+  float r;       // S_t / S_d
+  float S_t;     // sum_j 2^(z_j c - R_t) over the target row
+  int status;    // 0 valid, else ST_* bits
+  int greedy;
+  int pad;
+};
 
 struct KParams {
   const void* target;        // [B, k+1, V]
@@ -59,10 +72,12 @@ struct KParams {
   const float* uniforms;     // [B, k+1]
   float* out_p;              // [B, k] or null
   float* out_q;              // [B, k] or null
-  float* out_tv;             // [B, k] or null
+  float* out_tv;             // [B, k] or null (greedy units only; others in finalize)
   int32_t* ws_acc;           // [B, k]
-  int32_t* ws_y;             // [B, k+1]
-  int32_t* ws_status;        // [B, k+1]
+  int32_t* ws_y;             // [B, k+1] greedy tokens
+  UnitStat* ws_stat;         // [B, k+1]
+  float* ws_w;               // [B, k+1, items] residual (or target) mass per warp range
+  float* ws_p;               // [B, k+1, items] share of sum e_t per warp range
   int* flags;                // [0] invalid count, [1] wait timeout
   int B, k, V, Vs;
   int wv;                    // vectors per warp: ceil(ceil(Vs / EPV) / NWARP)
@@ -71,23 +86,18 @@ struct KParams {
   int tma;
 };
 
-struct alignas(16) X1 {       // one warp's part of exchange 1 (32 bytes)
+struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
   float m_t, m_d;              // maxima of the warp's range in the target / draft row
   float s_t, s_d;              // sums of 2^(z*c - ref(m)) over the range
   int i_t, i_d;                // lowest index of the maximum (T == 0)
   int pad0, pad1;
 };
-struct alignas(8) X2 {         // one warp's part of exchange 2 (8 bytes)
-  float w;                     // residual (or target) weight of the warp's range
-  int acc;                     // accept decision if the warp owns the drafted token, else -1
-};
 
 struct Small {
   unsigned long long bar;      // stage mbarrier
-  int pad0[2];
-  X1 x1[2][CMAX * NWARP];      // double-buffered exchange slots, written by peers
-  X2 x2[2][CMAX * NWARP];
-  float gz_t, gz_d;            // logits at the drafted token (owner CTA)
+  unsigned cnt;                // warps done copying the current stage
+  int pad0;
+  X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "bookkeeping area too small");
 
@@ -110,9 +120,6 @@ __device__ __forceinline__ void st_peer_x1(uint32_t a, const X1& v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(__float_as_uint(v.m_t)),
                "r"(__float_as_uint(v.m_d)), "r"(__float_as_uint(v.s_t)), "r"(__float_as_uint(v.s_d)) : "memory");
   asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a + 16), "r"(v.i_t), "r"(v.i_d) : "memory");
-}
-__device__ __forceinline__ void st_peer_x2(uint32_t a, const X2& v) {
-  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(__float_as_uint(v.w)), "r"(v.acc) : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) { asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory"); }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
@@ -140,7 +147,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, unsigned
 __device__ __forceinline__ float ex2(float x) { float y; asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x)); return y; }
 __device__ __forceinline__ float nanmax(float a, float b) { float y; asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b)); return y; }
 __device__ __forceinline__ float warp_max_nan(float v) { float y; asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(v)); return y; }
-__device__ __forceinline__ int warp_max_s32(int v) { int y; asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(y) : "r"(v)); return y; }
 // 2^n for an integer-valued n <= 0, exact (0 below the normal range)
 __device__ __forceinline__ float pow2_int(float n) {
   const int e = (int)n;
@@ -167,6 +173,17 @@ __device__ __forceinline__ float ref_of(float m, float c) {
 }
 
 // ------------------------------------------------------------ per-type access
+// Arrive on the stage counter; the last of NWARP warps returns true (acq_rel,
+// so every warp's reads of the stage happen before the caller's next copy).
+__device__ __forceinline__ bool stage_release_last(unsigned* cnt) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(saddr(cnt)) : "memory");
+  if (old == NWARP - 1) {
+    asm volatile("st.relaxed.cta.shared::cta.u32 [%0], 0;" ::"r"(saddr(cnt)) : "memory");
+    return true;
+  }
+  return false;
+}
 template <typename Tl> struct Lay;
 template <> struct Lay<float> {
   static constexpr int EPV = 4;
@@ -275,38 +292,58 @@ __device__ __forceinline__ void vec_weights(const uint4& t, const uint4& d, bool
   }
 }
 
+// One 16-byte vector v of a row slice read with plain loads (any alignment);
+// entries at or past slen, or when !valid, are -inf.
+template <typename Tl>
+__device__ __forceinline__ uint4 load_vec_direct(const void* slice, long long v, int slen, bool valid) {
+  constexpr int EPV = Lay<Tl>::EPV, ES = (int)sizeof(Tl);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int h = 0; h < 4 / ES; ++h) {   // 1 fp32 or 2 bf16 per 32-bit word
+      const long long idx = v * EPV + q * (4 / ES) + h;
+      const bool in = valid && idx < slen;
+      if (ES == 4) x = in ? ((const uint32_t*)slice)[idx] : 0xff800000u;
+      else x |= (in ? (uint32_t)((const uint16_t*)slice)[idx] : 0xff80u) << (16 * h);
+    }
+    w[q] = x;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ------------------------------------------------------------- fused kernel
 // Vector v of a CTA's slice (16 bytes: EPV logits) belongs to warp v / WV,
 // round (v % WV) / 32, lane v % 32, where WV = ceil(nvec / NWARP): every warp
-// owns a contiguous range of the vocabulary, and warps are ordered like the
-// vocabulary, so (rank, warp) partials are already in index order.
+// owns a contiguous range of the vocabulary, and (rank, warp) items are in
+// vocabulary order.
 template <typename Tl, int R>
 __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   extern __shared__ __align__(128) unsigned char smem[];
   Small& S = *reinterpret_cast<Small*>(smem);
-  float* wsm = reinterpret_cast<float*>(smem + SMALL_BYTES);                 // [R][NT] round weights
-  const uint4* stage_t = reinterpret_cast<const uint4*>(smem + SMALL_BYTES + R * NT * 4);
-  const uint4* stage_d = reinterpret_cast<const uint4*>(smem + SMALL_BYTES + R * NT * 4 + (size_t)P.Vs * ES);
+  const uint4* stage_t = reinterpret_cast<const uint4*>(smem + SMALL_BYTES);
+  const uint4* stage_d = reinterpret_cast<const uint4*>(smem + SMALL_BYTES + (size_t)P.Vs * ES);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned C = cl_size(), rank = cl_rank();
   const unsigned cid = cl_id(), ncl = cl_count();
   const int k = P.k, V = P.V, upc = P.units_per_chain;
-  const int items = (int)C * NWARP;                     // exchange items per cluster
+  const int items = (int)C * NWARP;
   const long long slice0 = (long long)rank * P.Vs;
   const int slen = (int)max(0LL, min((long long)P.Vs, (long long)V - slice0));
   const int nvec = (slen + EPV - 1) / EPV;
-  const int WV = P.wv;                                  // vectors per warp
-  const int vbeg = warp * WV;
-  const int vend = min(vbeg + WV, nvec);
+  const int vbeg = warp * P.wv;
+  const int vend = min(vbeg + P.wv, nvec);
   const long long n_units = (long long)P.B * upc;
   const uint32_t bar = saddr(&S.bar);
   const uint32_t stage_t_s = saddr(stage_t), stage_d_s = saddr(stage_d);
 
   if (tid == 0) {
     mbar_init(bar, 1);
+    S.cnt = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -319,7 +356,7 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
     trow = (long long)b * (k + 1) + ipos;
     drow = (long long)b * k + ipos;
   };
-  auto issue_load = [&](long long u) {   // thread 0 only
+  auto issue_load = [&](long long u) {   // one thread
     long long trow, drow; int ipos, b; bool pair;
     unit_rows(u, trow, drow, ipos, b, pair);
     if (slen > 0) {
@@ -335,14 +372,23 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   long long u = cid;
   if (P.tma && tid == 0 && u < n_units) issue_load(u);
   unsigned phase = 0;
-  int n1 = 0, n2 = 0;   // exchanges of each kind performed (select the slot set)
+  int n1 = 0;   // exchanges performed (selects the slot set)
 
   for (; u < n_units; u += ncl, phase ^= 1u) {
     long long trow, drow; int ipos, b; bool pair;
     unit_rows(u, trow, drow, ipos, b, pair);
 
-    // ---------------- bring this warp's vectors of the unit into registers
+    // ---------------- per-chain scalars (identical in every CTA of the cluster)
+    const float T = P.temperature[b];
+    const int x = pair && !P.tv_only ? P.tokens[(size_t)b * k + ipos] : 0;
+    const bool t_ok = T >= 0.0f && T <= 3.0e38f;   // false for NaN and inf
+    const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
+    const bool x_ok = !pair || P.tv_only || (x >= 0 && x < V);
+    const bool own_x = pair && !P.tv_only && x_ok && (long long)x >= slice0 && (long long)x < slice0 + slen;
+
+    // ---------------- this warp's vectors of the unit into registers
     uint4 rt[R], rd[R];
+    float gz_t = 0.0f, gz_d = 0.0f;   // logits at the drafted token (thread 0 of its owner CTA)
     if (P.tma) {
       mbar_wait_bounded(bar, phase, P.flags);
 #pragma unroll
@@ -351,61 +397,28 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
         rt[j] = v < vend ? stage_t[v] : Lay<Tl>::neg_inf();
         rd[j] = (pair && v < vend) ? stage_d[v] : Lay<Tl>::neg_inf();
       }
+      if (tid == 0 && own_x) {
+        gz_t = Lay<Tl>::load_scalar(stage_t, x - slice0);
+        gz_d = Lay<Tl>::load_scalar(stage_d, x - slice0);
+      }
+      __syncwarp();
+      if (lane == 0 && stage_release_last(&S.cnt) && u + ncl < n_units) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_load(u + ncl);
+      }
     } else {
       const char* tb = (const char*)P.target + ((size_t)trow * V + slice0) * ES;
       const char* db = (const char*)P.draft + ((size_t)drow * V + slice0) * ES;
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         const int v = vbeg + j * 32 + lane;
-        const bool vin = v < vend;
-        uint32_t wt[4], wd[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t xt = 0, xd = 0;
-#pragma unroll
-          for (int h = 0; h < 4 / ES; ++h) {   // 1 fp32 or 2 bf16 per 32-bit word
-            const int e = q * (4 / ES) + h;
-            const long long idx = (long long)v * EPV + e;
-            const bool in = vin && idx < slen;
-            if (ES == 4) {
-              xt = in ? ((const uint32_t*)tb)[idx] : 0xff800000u;
-              xd = (pair && in) ? ((const uint32_t*)db)[idx] : 0xff800000u;
-            } else {
-              const uint32_t bt = in ? ((const uint16_t*)tb)[idx] : 0xff80u;
-              const uint32_t bd = (pair && in) ? ((const uint16_t*)db)[idx] : 0xff80u;
-              xt |= bt << (16 * h); xd |= bd << (16 * h);
-            }
-          }
-          wt[q] = xt; wd[q] = xd;
-        }
-        rt[j] = make_uint4(wt[0], wt[1], wt[2], wt[3]);
-        rd[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        rt[j] = load_vec_direct<Tl>(tb, v, slen, v < vend);
+        rd[j] = load_vec_direct<Tl>(db, v, slen, pair && v < vend);
       }
-    }
-
-    // ---------------- per-chain scalars (identical in every CTA of the cluster)
-    const float T = P.temperature[b];
-    const int x = pair && !P.tv_only ? P.tokens[(size_t)b * k + ipos] : 0;
-    const float u_acc = pair && !P.tv_only ? P.uniforms[(size_t)b * (k + 1) + ipos] : 0.0f;
-    const float u_fin = P.tv_only ? 0.0f : P.uniforms[(size_t)b * (k + 1) + k];
-    const bool t_ok = T >= 0.0f && T <= 3.0e38f;   // false for NaN and inf
-    const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
-    const bool x_ok = !pair || P.tv_only || (x >= 0 && x < V);
-    const bool own_x = pair && !P.tv_only && x_ok && (long long)x >= slice0 && (long long)x < slice0 + slen;
-    if (tid == 0 && own_x) {
-      const long long lx = x - slice0;
-      if (P.tma) {
-        S.gz_t = Lay<Tl>::load_scalar(stage_t, lx);
-        S.gz_d = Lay<Tl>::load_scalar(stage_d, lx);
-      } else {
-        S.gz_t = Lay<Tl>::load_scalar(P.target, (long long)trow * V + x);
-        S.gz_d = Lay<Tl>::load_scalar(P.draft, (long long)drow * V + x);
+      if (tid == 0 && own_x) {
+        gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
+        gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
       }
-    }
-    __syncthreads();   // stage fully consumed; gathered values visible
-    if (P.tma && tid == 0 && u + ncl < n_units) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue_load(u + ncl);
     }
 
     const float c = greedy ? 0.0f : fminf(__fdiv_rn(LOG2E_F, T), 3.0e38f);
@@ -422,6 +435,7 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
     mine.m_d = pair ? warp_max_nan(tm_d) : -INFINITY;
     mine.i_t = 0x7fffffff; mine.i_d = 0x7fffffff;
     mine.s_t = 0.0f; mine.s_d = 0.0f;
+    mine.pad0 = 0; mine.pad1 = 0;
     if (greedy) {
       int ci_t = 0x7fffffff, ci_d = 0x7fffffff;   // lowest global index holding the warp maximum
 #pragma unroll
@@ -461,24 +475,21 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
     {
       X1 z;
       z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
+      z.pad0 = 0; z.pad1 = 0;
       ia = lane < items ? S.x1[set1][lane] : z;
       ib = lane + 32 < items ? S.x1[set1][lane + 32] : z;
     }
     const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
     const float M_d = warp_max_nan(nanmax(ia.m_d, ib.m_d));
     int A_t = 0, A_d = 0;
-    float S_t = 0.0f, S_d = 0.0f;
-    float pa = 0.0f, pb = 0.0f;   // items' shares of sum_j e_t (fallback draw)
-    float R_t = 0.0f, R_d = 0.0f;
+    float S_t = 0.0f, S_d = 0.0f, R_t = 0.0f, R_d = 0.0f;
     if (greedy) {
       A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
       A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
     } else {
       R_t = ref_of(M_t, c);
       R_d = ref_of(M_d, c);
-      pa = ia.s_t * pow2_int(ref_of(ia.m_t, c) - R_t);
-      pb = ib.s_t * pow2_int(ref_of(ib.m_t, c) - R_t);
-      S_t = warp_sum_f32(pa + pb);
+      S_t = warp_sum_f32(ia.s_t * pow2_int(ref_of(ia.m_t, c) - R_t) + ib.s_t * pow2_int(ref_of(ib.m_t, c) - R_t));
       S_d = warp_sum_f32(ia.s_d * pow2_int(ref_of(ia.m_d, c) - R_d) + ib.s_d * pow2_int(ref_of(ib.m_d, c) - R_d));
     }
     bool row_ok = isfinite(M_t) && (!pair || isfinite(M_d));
@@ -489,93 +500,137 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
     const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
     const size_t ui = (size_t)b * (k + 1) + ipos;   // unit index within [B, k+1]
     const size_t pi = (size_t)b * k + ipos;         // position index within [B, k]
+    const float r_f = pair && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
 
-    if (status != 0 || greedy) {
-      if (rank == 0 && tid == 0) {
-        if (!P.tv_only) {
-          P.ws_status[ui] = status;
-          if (status == 0) {
-            P.ws_y[ui] = A_t;
-            if (pair) {
-              P.ws_acc[pi] = x == A_t;
-              if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
-              if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
-            }
+    if (rank == 0 && tid == 0) {
+      UnitStat st;
+      st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
+      st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
+      P.ws_stat[ui] = st;
+      if (status != 0 || greedy) {
+        if (!P.tv_only && status == 0) {
+          P.ws_y[ui] = A_t;
+          if (pair) {
+            P.ws_acc[pi] = x == A_t;
+            if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
+            if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
           }
-        } else if (status != 0) {
-          atomicAdd(&P.flags[0], 1);
         }
         if (pair && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
       }
-      continue;   // cluster-uniform: every CTA took the same branch
     }
+    if (status != 0 || greedy) continue;   // cluster-uniform
 
-    // ---------------- pass B: residual (pair) or target (bonus) weights, unscaled
+    // ---------------- pass B: residual (pair) or target (bonus) mass of this warp's range
     const u64 cc = pk(c, c);
     const u64 nrt = pk(-R_t, -R_t), nrd = pk(-R_d, -R_d);
-    const float r_f = pair ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
     const u64 nr = pk(-r_f, -r_f);
     float wthr = 0.0f;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const float wj = pair ? vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr)
-                            : vec_weight_sum<Tl, false>(rt[j], rd[j], cc, nrt, nrd, nr);
-      wsm[j * NT + tid] = wj;
-      wthr += wj;
+      wthr += pair ? vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr)
+                   : vec_weight_sum<Tl, false>(rt[j], rd[j], cc, nrt, nrd, nr);
     }
-    X2 mine2;
-    mine2.w = warp_sum_f32(wthr);
-    mine2.acc = -1;
-    if (own_x && tid == 0) {   // accept test at the drafted token (owner CTA, one thread)
-      const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
+    const float wwarp = warp_sum_f32(wthr);
+    if (lane == 0) {
+      const size_t it = ui * ITEMS_MAX + rank * NWARP + warp;
+      P.ws_w[it] = wwarp;
+      P.ws_p[it] = mine.s_t * pow2_int(ref_of(mine.m_t, c) - R_t);   // this range's part of S_t
+    }
+    if (own_x && tid == 0) {   // accept test at the drafted token
+      const float lpx = fmaf(gz_t, c, -R_t), lqx = fmaf(gz_d, c, -R_d);
       const float ratio = exp2f(lpx - lqx) * (S_d / S_t);
-      mine2.acc = u_acc < ratio ? 1 : 0;
-      P.ws_acc[pi] = mine2.acc;
+      const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
+      P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
       if (P.out_p) P.out_p[pi] = exp2f(lpx) / S_t;
       if (P.out_q) P.out_q[pi] = exp2f(lqx) / S_d;
     }
-    mine2.acc = __shfl_sync(FULL, mine2.acc, 0);
+  }
+  cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
+}
 
-    // ---------------- exchange 2: per-warp residual mass and the accept decision
-    const int set2 = n2 & 1;
-    if (lane < (int)C) st_peer_x2(peer_addr(saddr(&S.x2[set2][rank * NWARP + warp]), lane), mine2);
-    cluster_sync_all();
-    ++n2;
+// ------------------------------------------------------------ finalize kernel
+struct FParams {
+  const void* target;
+  const void* draft;
+  const int32_t* tokens;
+  const float* uniforms;
+  const int32_t* ws_acc;
+  const int32_t* ws_y;
+  const UnitStat* ws_stat;
+  const float* ws_w;
+  const float* ws_p;
+  int32_t* out_tokens;
+  int32_t* out_tau;
+  float* out_tv;
+  int* flags;
+  int B, k, V, Vs, wv, items, tma, tv_only;
+};
 
-    // lane l holds items 2l and 2l+1 (vocabulary order)
-    X2 ja, jb;
-    ja.w = 0.0f; ja.acc = -1; jb.w = 0.0f; jb.acc = -1;
-    if (2 * lane < items) ja = S.x2[set2][2 * lane];
-    if (2 * lane + 1 < items) jb = S.x2[set2][2 * lane + 1];
-    const int acc_all = warp_max_s32(max(ja.acc, jb.acc));
-    const float res_total = warp_sum_f32(ja.w + jb.w);                    // S_t * TV
-    const bool fallback = pair && !(res_total > 0.0f);                     // zero residual: draw from p
-    double wa = ja.w, wb = jb.w;
-    if (fallback) {   // the p shares of items 2l, 2l+1 live in lanes l and l+16 (as items l, l+32)
-      const int ka = 2 * lane, kb = 2 * lane + 1;
-      const float a0 = __shfl_sync(FULL, pa, ka & 31), a1 = __shfl_sync(FULL, pb, ka & 31);
-      const float b0 = __shfl_sync(FULL, pa, kb & 31), b1 = __shfl_sync(FULL, pb, kb & 31);
-      wa = ka < items ? (ka < 32 ? a0 : a1) : 0.0f;
-      wb = kb < items ? (kb < 32 ? b0 : b1) : 0.0f;
+// One warp per chain: tau by ballot, TV from the per-range masses, and the
+// inverse-CDF draw of the final token (re-reading only the owning range).
+template <typename Tl, int R>
+__global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
+  constexpr int EPV = Lay<Tl>::EPV;
+  constexpr int ES = (int)sizeof(Tl);
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (b >= F.B) return;
+  const int k = F.k, items = F.items;
+  const size_t ub = (size_t)b * (k + 1);
+  const int npos = F.tv_only ? k : k + 1;
+  const int st = lane < npos ? F.ws_stat[ub + lane].status : 0;
+  const bool bad = __any_sync(FULL, st != 0);
+
+  // TV of every valid, non-greedy position
+  if (F.out_tv) {
+    for (int i = 0; i < k; ++i) {
+      const UnitStat us = F.ws_stat[ub + i];
+      if (us.status != 0 || us.greedy) continue;
+      const float* w = F.ws_w + (ub + i) * ITEMS_MAX;
+      float v = (lane < items ? w[lane] : 0.0f) + (lane + 32 < items ? w[lane + 32] : 0.0f);
+      v = warp_sum_f32(v);
+      if (lane == 0) F.out_tv[(size_t)b * k + i] = v / us.S_t;
     }
+  }
+  if (bad && lane == 0) atomicAdd(&F.flags[0], 1);
+  if (F.tv_only) return;
+  if (bad) {
+    if (lane <= k) F.out_tokens[ub + lane] = -1;
+    if (lane == 0) F.out_tau[b] = -1;
+    return;
+  }
+  const int a = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
+  const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
+  const int tau = rej ? __ffs(rej) - 1 : k;
+  const bool pair = tau < k;
+  const size_t uu = ub + tau;
+  const UnitStat us = F.ws_stat[uu];
+  int y = 0;
+  if (us.greedy) {
+    y = F.ws_y[uu];
+  } else {
+    // ---- which (CTA, warp) range holds u * total mass
+    const float* wp = F.ws_w + uu * ITEMS_MAX;
+    const float* pp = F.ws_p + uu * ITEMS_MAX;
+    const int ka = 2 * lane, kb = 2 * lane + 1;
+    float fa = ka < items ? wp[ka] : 0.0f, fb = kb < items ? wp[kb] : 0.0f;
+    const bool fallback = pair && !(warp_sum_f32(fa + fb) > 0.0f);   // zero residual: draw from p
+    if (fallback) {
+      fa = ka < items ? pp[ka] : 0.0f;
+      fb = kb < items ? pp[kb] : 0.0f;
+    }
+    const double wa = fa, wb = fb;
     double incl = wa + wb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += y;
+      const double t = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += t;
     }
     double excl = __shfl_up_sync(FULL, incl, 1);
     if (lane == 0) excl = 0.0;
     const double total = __shfl_sync(FULL, incl, 31);
-
-    if (rank == 0 && tid == 0) {
-      if (pair && P.out_tv) P.out_tv[pi] = res_total / S_t;
-      if (!P.tv_only) P.ws_status[ui] = 0;
-    }
-    if (P.tv_only || (pair && acc_all == 1)) continue;   // no draw needed for this unit
-
-    // ---------------- inverse-CDF draw: which (CTA, warp) holds u * total
-    const double tt = (double)u_fin * total;
+    const double tt = (double)F.uniforms[ub + k] * total;   // the final draw uses u[b, k]
     const bool ca = wa > 0.0 && tt < excl + wa;
     const bool cb = wb > 0.0 && tt < incl;
     const unsigned hit = __ballot_sync(FULL, ca || cb);
@@ -595,15 +650,34 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
       tloc = 0.0;
       over = true;
     }
-    if (item != (int)rank * NWARP + warp) continue;   // only the owning warp draws
-
-    // Owner warp: round totals, then the lane, then the element.
+    // ---- re-read the owning range and finish the draw there
+    const int crank = item / NWARP, cwarp = item % NWARP;
+    const long long slice0 = (long long)crank * F.Vs;
+    const int slen = (int)max(0LL, min((long long)F.Vs, (long long)F.V - slice0));
+    const int nvec = (slen + EPV - 1) / EPV;
+    const int vbeg = cwarp * F.wv, vend = min(vbeg + F.wv, nvec);
     const bool use_pair = pair && !fallback;
-    float wl[R];
+    const char* tb = (const char*)F.target + ((size_t)(ub + tau) * F.V + slice0) * ES;
+    const char* db = (const char*)F.draft + (((size_t)b * k + (pair ? tau : 0)) * F.V + slice0) * ES;
+    uint4 rt[R], rd[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      wl[j] = fallback ? vec_weight_sum<Tl, false>(rt[j], rd[j], cc, nrt, nrd, nr) : wsm[j * NT + tid];
+      const int v = vbeg + j * 32 + lane;
+      if (F.tma) {
+        rt[j] = v < vend ? __ldg(reinterpret_cast<const uint4*>(tb) + v) : Lay<Tl>::neg_inf();
+        rd[j] = (use_pair && v < vend) ? __ldg(reinterpret_cast<const uint4*>(db) + v) : Lay<Tl>::neg_inf();
+      } else {
+        rt[j] = load_vec_direct<Tl>(tb, v, slen, v < vend);
+        rd[j] = load_vec_direct<Tl>(db, v, slen, use_pair && v < vend);
+      }
     }
+    const u64 cc = pk(us.c, us.c);
+    const u64 nrt = pk(-us.R_t, -us.R_t), nrd = pk(-us.R_d, -us.R_d), nr = pk(-us.r, -us.r);
+    float wl[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      wl[j] = use_pair ? vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr)
+                       : vec_weight_sum<Tl, false>(rt[j], rd[j], cc, nrt, nrd, nr);
     int jstar = -1, jlast = -1;
     double tin = 0.0, run = 0.0;
 #pragma unroll
@@ -614,22 +688,23 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
       run += tj;
     }
     if (jstar < 0) { jstar = jlast; over = true; }
-    if (jstar < 0) continue;   // nothing positive (cannot happen for a valid owner)
+    if (jstar < 0) jstar = 0;   // no positive weight in the range (cannot happen for a valid unit)
     float mw = 0.0f;
 #pragma unroll
     for (int j = 0; j < R; ++j) if (j == jstar) mw = wl[j];
     double inc = (double)mw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(FULL, inc, o);
-      if (lane >= o) inc += y;
+      const double t = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += t;
     }
     const unsigned h2 = __ballot_sync(FULL, !over && mw > 0.0f && tin < inc);
     const unsigned p2 = __ballot_sync(FULL, mw > 0.0f);
     int lstar;
     if (h2) lstar = __ffs(h2) - 1;
-    else { lstar = 31 - __clz(p2); over = true; }
+    else { lstar = p2 ? 31 - __clz(p2) : 0; over = true; }
     const double t2 = tin - (__shfl_sync(FULL, inc, lstar) - (double)__shfl_sync(FULL, mw, lstar));
+    int estar = -1;
     if (lane == lstar) {
       float w[EPV];
 #pragma unroll
@@ -637,7 +712,7 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
 #pragma unroll
       for (int j = 0; j < R; ++j)
         if (j == jstar) vec_weights<Tl>(rt[j], rd[j], use_pair, cc, nrt, nrd, nr, w);
-      int estar = -1, elast = 0;
+      int elast = 0;
       double run2 = 0.0;
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
@@ -646,61 +721,33 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
         run2 += (double)w[e];
       }
       if (estar < 0) estar = elast;
-      P.ws_y[ui] = (int)slice0 + (vbeg + jstar * 32 + lstar) * EPV + estar;
     }
-  }
-  cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
-}
-
-// ------------------------------------------------------------ finalize kernel
-struct FParams {
-  const int32_t* tokens;
-  const int32_t* ws_acc;
-  const int32_t* ws_y;
-  const int32_t* ws_status;
-  int32_t* out_tokens;
-  int32_t* out_tau;
-  int* flags;
-  int B, k;
-};
-
-__global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (b >= F.B) return;
-  const int k = F.k;
-  const int st = lane <= k ? F.ws_status[(size_t)b * (k + 1) + lane] : 0;
-  const bool bad = __any_sync(FULL, st != 0);
-  const int a = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
-  const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
-  const int tau = rej ? __ffs(rej) - 1 : k;
-  if (bad) {
-    if (lane <= k) F.out_tokens[(size_t)b * (k + 1) + lane] = -1;
-    if (lane == 0) { F.out_tau[b] = -1; atomicAdd(&F.flags[0], 1); }
-    return;
+    estar = __shfl_sync(FULL, estar, lstar);
+    y = (int)slice0 + (vbeg + jstar * 32 + lstar) * EPV + estar;
   }
   if (lane <= k) {
     int tok = -1;
     if (lane < tau) tok = F.tokens[(size_t)b * k + lane];
-    else if (lane == tau) tok = F.ws_y[(size_t)b * (k + 1) + tau];
-    F.out_tokens[(size_t)b * (k + 1) + lane] = tok;
+    else if (lane == tau) tok = y;
+    F.out_tokens[ub + lane] = tok;
   }
   if (lane == 0) F.out_tau[b] = tau;
 }
 
 typedef void (*FusedFn)(const KParams);
+typedef void (*FinalFn)(const FParams);
 constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10};
 constexpr int N_R = 6;
 
 template <typename Tl>
-FusedFn pick_kernel(int r) {
+void pick_kernels(int r, FusedFn& f, FinalFn& g) {
   switch (r) {
-    case 1: return sv_fused_kernel<Tl, 1>;
-    case 2: return sv_fused_kernel<Tl, 2>;
-    case 4: return sv_fused_kernel<Tl, 4>;
-    case 6: return sv_fused_kernel<Tl, 6>;
-    case 8: return sv_fused_kernel<Tl, 8>;
-    default: return sv_fused_kernel<Tl, 10>;
+    case 1: f = sv_fused_kernel<Tl, 1>; g = sv_finalize_kernel<Tl, 1>; break;
+    case 2: f = sv_fused_kernel<Tl, 2>; g = sv_finalize_kernel<Tl, 2>; break;
+    case 4: f = sv_fused_kernel<Tl, 4>; g = sv_finalize_kernel<Tl, 4>; break;
+    case 6: f = sv_fused_kernel<Tl, 6>; g = sv_finalize_kernel<Tl, 6>; break;
+    case 8: f = sv_fused_kernel<Tl, 8>; g = sv_finalize_kernel<Tl, 8>; break;
+    default: f = sv_fused_kernel<Tl, 10>; g = sv_finalize_kernel<Tl, 10>; break;
   }
 }
 
@@ -714,9 +761,12 @@ struct spec_verify_ctx {
   int C, Vs, R, wv, n_clusters, tma_ok;
   size_t smem;
   FusedFn kernel;
+  FinalFn finalize;
   int32_t* ws_acc;
   int32_t* ws_y;
-  int32_t* ws_status;
+  UnitStat* ws_stat;
+  float* ws_w;
+  float* ws_p;
   int* d_flags;
   // host staging (SV_FLAG_HOST_STAGING)
   void* st_target;
@@ -738,7 +788,7 @@ static constexpr int TIMING_RING = 4096;
 
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
-  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_status, h->d_flags, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
+  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
                   h->st_unif, h->st_out_tokens, h->st_out_tau, h->st_out_p, h->st_out_q, h->st_out_tv};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -773,6 +823,20 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
     if (cudaEventRecord(h->ev[2 * h->ev_n + 1], s) != cudaSuccess) return SV_ERR_CUDA;
     h->ev_n++;
   }
+  return SV_OK;
+}
+
+static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* tokens, int32_t* out_tokens,
+                           int32_t* out_tau, cudaStream_t s) {
+  FParams F;
+  memset(&F, 0, sizeof F);
+  F.target = P.target; F.draft = P.draft; F.tokens = tokens; F.uniforms = P.uniforms;
+  F.ws_acc = P.ws_acc; F.ws_y = P.ws_y; F.ws_stat = P.ws_stat; F.ws_w = P.ws_w; F.ws_p = P.ws_p;
+  F.out_tokens = out_tokens; F.out_tau = out_tau; F.out_tv = P.out_tv; F.flags = P.flags;
+  F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.wv = P.wv; F.items = h->C * NWARP; F.tma = P.tma;
+  F.tv_only = P.tv_only;
+  h->finalize<<<(P.B + 7) / 8, 256, 0, s>>>(F);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -821,8 +885,9 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   h->max_batch = max_batch; h->k = k; h->V = vocab; h->dtype = logit_dtype; h->flags = flags;
   h->C = C; h->Vs = (int)Vs; h->R = R; h->wv = (int)wv;
   h->tma_ok = ((size_t)vocab * es) % 16 == 0 && !(flags & SV_FLAG_NO_TMA);
-  h->smem = SMALL_BYTES + (size_t)R * NT * 4 + 2 * (size_t)Vs * es;
-  h->kernel = logit_dtype == SV_FP32 ? pick_kernel<float>(R) : pick_kernel<__nv_bfloat16>(R);
+  h->smem = SMALL_BYTES + 2 * (size_t)Vs * es;
+  if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->finalize);
+  else pick_kernels<__nv_bfloat16>(R, h->kernel, h->finalize);
   if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
     free_ctx(h);
     return SV_ERR_CUDA;
@@ -851,7 +916,9 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   const size_t mb = (size_t)(max_batch > 0 ? max_batch : 1);
   bool ok = cudaMalloc(&h->ws_acc, mb * k * sizeof(int32_t)) == cudaSuccess &&
             cudaMalloc(&h->ws_y, mb * (k + 1) * sizeof(int32_t)) == cudaSuccess &&
-            cudaMalloc(&h->ws_status, mb * (k + 1) * sizeof(int32_t)) == cudaSuccess &&
+            cudaMalloc(&h->ws_stat, mb * (k + 1) * sizeof(UnitStat)) == cudaSuccess &&
+            cudaMalloc(&h->ws_w, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
+            cudaMalloc(&h->ws_p, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess;
   if (ok && (flags & SV_FLAG_HOST_STAGING)) {
     const size_t rowb = (size_t)vocab * es;
@@ -906,18 +973,14 @@ int spec_verify(spec_verify_t h, int batch, const void* target_logits, const voi
   memset(&P, 0, sizeof P);
   P.target = target_logits; P.draft = draft_logits; P.tokens = draft_tokens; P.temperature = temperature;
   P.uniforms = uniforms; P.out_p = out_p_draft; P.out_q = out_q_draft; P.out_tv = out_tv;
-  P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_status = h->ws_status; P.flags = h->d_flags;
+  P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
+  P.flags = h->d_flags;
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
   int rc = launch_fused(h, P, (long long)batch * (h->k + 1), s);
   if (rc != SV_OK) return rc;
-  FParams F;
-  F.tokens = draft_tokens; F.ws_acc = h->ws_acc; F.ws_y = h->ws_y; F.ws_status = h->ws_status;
-  F.out_tokens = out_tokens; F.out_tau = out_tau; F.flags = h->d_flags; F.B = batch; F.k = h->k;
-  sv_finalize_kernel<<<(batch + 7) / 8, 256, 0, s>>>(F);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-  return SV_OK;
+  return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s);
 }
 
 int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
@@ -931,11 +994,15 @@ int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const 
   KParams P;
   memset(&P, 0, sizeof P);
   P.target = target_logits; P.draft = draft_logits; P.temperature = temperature; P.out_tv = out_tv;
-  P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_status = h->ws_status; P.flags = h->d_flags;
+  P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
+  P.flags = h->d_flags;
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k; P.tv_only = 1;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
-  return launch_fused(h, P, (long long)batch * h->k, (cudaStream_t)cuda_stream);
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  int rc = launch_fused(h, P, (long long)batch * h->k, s);
+  if (rc != SV_OK) return rc;
+  return launch_finalize(h, P, nullptr, nullptr, nullptr, s);
 }
 
 int spec_verify_host(spec_verify_t h, int batch, const void* host_target_logits, const void* host_draft_logits,
@@ -989,7 +1056,7 @@ int spec_verify_info(spec_verify_t h, int* cluster_size, int* n_clusters, int* r
   if (n_clusters) *n_clusters = h->n_clusters;
   if (rounds) *rounds = h->R;
   if (tma) *tma = h->tma_ok;
-  if (launches_per_call) *launches_per_call = 2;
+  if (launches_per_call) *launches_per_call = 2;   // verification kernel + finalize kernel
   return SV_OK;
 }
 
