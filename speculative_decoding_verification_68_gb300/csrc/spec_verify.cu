@@ -16,9 +16,10 @@
 //   * Pass A (registers): per-row maximum, then sum of exp2(z*c - R) with an
 //     integer reference R = ceil(max*c), c = log2(e)/T.  Integer references
 //     make every rescale between warps and CTAs an exact power of two.
-//   * Exchange (DSMEM push + one cluster barrier per unit): every warp pushes
-//     its (max, sum) of both rows to every CTA; each warp merges the C*8
-//     parts in the same order, so all CTAs hold identical row statistics.
+//   * Exchange (DSMEM, no cluster barrier): every warp sends its (max, sum) of
+//     both rows to every CTA with st.async, which completes the bytes on the
+//     receiver's mbarrier; each warp merges the C*8 parts in the same order,
+//     so all CTAs hold identical row statistics.
 //   * Pass B (registers): with e_j = 2^(z_j*c - R) and r = S_t/S_d, the
 //     residual weight w_j = max(0, e_t - r*e_d) = S_t * max(0, p_j - q_j) (one
 //     rounding, exactly zero for identical rows).  Each warp writes the sum of
@@ -95,7 +96,9 @@ struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
 
 struct Small {
   unsigned long long bar;      // stage mbarrier
+  unsigned long long xbar[2];  // exchange mbarriers, one per slot set (peers complete their bytes)
   unsigned cnt;                // warps done copying the current stage
+  float gz_t, gz_d;            // logits at the drafted token (thread 0 of the owner CTA)
   int pad0;
   X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
 };
@@ -121,6 +124,15 @@ __device__ __forceinline__ void st_peer_x1(uint32_t a, const X1& v) {
                "r"(__float_as_uint(v.m_d)), "r"(__float_as_uint(v.s_t)), "r"(__float_as_uint(v.s_d)) : "memory");
   asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a + 16), "r"(v.i_t), "r"(v.i_d) : "memory");
 }
+// Asynchronous remote store of one exchange part; completes its 32 bytes on
+// the receiver's mbarrier (no fence or barrier on the sender's side).
+__device__ __forceinline__ void st_async_x1(uint32_t slot, const X1& v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(slot), "r"(__float_as_uint(v.m_t)), "r"(__float_as_uint(v.m_d)), "r"(__float_as_uint(v.s_t)),
+               "r"(__float_as_uint(v.s_d)), "r"(rbar) : "memory");
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(slot + 16), "r"(v.i_t), "r"(v.i_d), "r"(v.pad0), "r"(v.pad1), "r"(rbar) : "memory");
+}
 __device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) { asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory"); }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
@@ -136,6 +148,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, unsigned parity) {
 __device__ __forceinline__ void mbar_wait_bounded(uint32_t a, unsigned parity, int* flags) {
   for (int it = 0; it < (1 << 22); ++it) {
     if (mbar_try(a, parity)) return;
+    if ((it & 255) == 255 && *(volatile int*)&flags[1]) return;
+  }
+  atomicExch(&flags[1], 1);
+}
+// Bounded wait for data that peers of the cluster deliver (acquire at cluster scope).
+__device__ __forceinline__ void mbar_wait_cluster_bounded(uint32_t a, unsigned parity, int* flags) {
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+    if (ok) return;
     if ((it & 255) == 255 && *(volatile int*)&flags[1]) return;
   }
   atomicExch(&flags[1], 1);
@@ -313,238 +336,332 @@ __device__ __forceinline__ uint4 load_vec_direct(const void* slice, long long v,
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Running maximum over vectors (NaN-propagating).
+template <typename Tl> struct MaxAcc;
+template <> struct MaxAcc<float> {
+  float m = -INFINITY;
+  __device__ __forceinline__ void add(const uint4& v) {
+    m = nanmax(m, nanmax(nanmax(__uint_as_float(v.x), __uint_as_float(v.y)), nanmax(__uint_as_float(v.z), __uint_as_float(v.w))));
+  }
+  __device__ __forceinline__ float get() const { return m; }
+};
+template <> struct MaxAcc<__nv_bfloat16> {
+  __nv_bfloat162 m;
+  __device__ __forceinline__ MaxAcc() { const uint32_t n = 0xff80ff80u; m = *reinterpret_cast<const __nv_bfloat162*>(&n); }
+  __device__ __forceinline__ void add(const uint4& v) {
+    m = __hmax2_nan(m, *reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    m = __hmax2_nan(m, *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    m = __hmax2_nan(m, *reinterpret_cast<const __nv_bfloat162*>(&v.z));
+    m = __hmax2_nan(m, *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+  }
+  __device__ __forceinline__ float get() const { return nanmax(__low2float(m), __high2float(m)); }
+};
+
+// Sum of 2^(z*c + nref) over R vectors with independent packed accumulators.
+template <typename Tl, int R>
+__device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr) {
+  u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    float x0, x1, x2, x3;
+    if constexpr (sizeof(Tl) == 4) {
+      upk(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr), x0, x1);
+      upk(fma2(pk(__uint_as_float(v[j].z), __uint_as_float(v[j].w)), cc, nr), x2, x3);
+      if (j & 1) { a2 = add2(a2, pk(ex2(x0), ex2(x1))); a3 = add2(a3, pk(ex2(x2), ex2(x3))); }
+      else { a0 = add2(a0, pk(ex2(x0), ex2(x1))); a1 = add2(a1, pk(ex2(x2), ex2(x3))); }
+    } else {
+      float x4, x5, x6, x7;
+      upk(fma2(pk(bf_lo(v[j].x), bf_hi(v[j].x)), cc, nr), x0, x1);
+      upk(fma2(pk(bf_lo(v[j].y), bf_hi(v[j].y)), cc, nr), x2, x3);
+      upk(fma2(pk(bf_lo(v[j].z), bf_hi(v[j].z)), cc, nr), x4, x5);
+      upk(fma2(pk(bf_lo(v[j].w), bf_hi(v[j].w)), cc, nr), x6, x7);
+      a0 = add2(a0, pk(ex2(x0), ex2(x1)));
+      a1 = add2(a1, pk(ex2(x2), ex2(x3)));
+      a2 = add2(a2, pk(ex2(x4), ex2(x5)));
+      a3 = add2(a3, pk(ex2(x6), ex2(x7)));
+    }
+  }
+  float l0, h0;
+  upk(add2(add2(a0, a1), add2(a2, a3)), l0, h0);
+  return l0 + h0;
+}
+
 // ------------------------------------------------------------- fused kernel
 // Vector v of a CTA's slice (16 bytes: EPV logits) belongs to warp v / WV,
 // round (v % WV) / 32, lane v % 32, where WV = ceil(nvec / NWARP): every warp
 // owns a contiguous range of the vocabulary, and (rank, warp) items are in
-// vocabulary order.
+// vocabulary order.  In shared memory each warp's range of each row has its
+// own block of R*32 vectors; the tail past the range stays -inf, so the
+// copy into registers needs no bounds checks.
+struct Geo {
+  unsigned C, rank;
+  int items;
+  long long slice0;
+  int slen, nvec, vbeg, vend;
+};
+
+// Bulk copies of one unit into the warp blocks of the stage, issued by one
+// whole warp: lane 0 arms the mbarrier with the byte count, then lane w
+// copies warp w's range of the target row and lane 8 + w that of the draft row.
 template <typename Tl, int R>
-__global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
+__device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, long long u, uint32_t bar,
+                                                const unsigned char* stage) {
+  constexpr int ES = (int)sizeof(Tl);
+  const int lane = threadIdx.x & 31;
+  const int upc = P.units_per_chain, k = P.k;
+  const int b = (int)(u / upc), ipos = (int)(u % upc);
+  const bool pair = ipos < k;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic accesses of the stage first
+  const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
+  if (lane == 0) {
+    const unsigned bytes = (unsigned)g.nvec * 16u;
+    if (bytes > 0) mbar_expect_tx(bar, pair ? 2 * bytes : bytes);
+    else mbar_arrive(bar);
+  }
+  __syncwarp();
+  const int w = lane & 7, row = lane >> 3;
+  if (lane < 16 && (row == 0 || pair)) {
+    const int vb = w * P.wv;
+    const int len = max(0, min(P.wv, g.nvec - vb));
+    if (len > 0) {
+      const char* src = (const char*)(row == 0 ? P.target : P.draft) +
+                        ((size_t)(row == 0 ? trow : drow) * P.V + g.slice0) * ES + (size_t)vb * 16;
+      const uint32_t dst = saddr(stage + ((size_t)(row * NWARP + w) * R * 32) * 16);
+      bulk_g2s(dst, src, (unsigned)len * 16u, bar);
+    }
+  }
+}
+
+template <typename Tl, int R, bool PAIR>
+__device__ __forceinline__ void process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
+                                             const Geo& g, long long u, int b, int ipos, long long trow,
+                                             long long drow, unsigned phase, int& n1, const uint32_t bar,
+                                             const unsigned char* smem_stage, long long next_u, bool tma_next) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k, V = P.V;
+
+  // per-chain scalars: issued before the stage wait so their latency overlaps it
+  const float T = P.temperature[b];
+  const int x = PAIR && !P.tv_only ? P.tokens[(size_t)b * k + ipos] : 0;
+
+  // ---------------- this warp's vectors of the unit into registers
+  uint4 rt[R], rd[R];
+  bool own_x = false;
+  if (P.tma) {
+    mbar_wait_bounded(bar, phase, P.flags);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      rt[j] = blk_t[j * 32 + lane];
+      if (PAIR) rd[j] = blk_d[j * 32 + lane];
+    }
+    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0 && (long long)x < g.slice0 + g.slen;
+    if (PAIR && tid == 0 && own_x) {
+      const int lx = (int)(x - g.slice0);
+      const int lv = lx / EPV, wb = lv / P.wv, iv = lv - wb * P.wv;
+      const unsigned char* bt = smem_stage + ((size_t)(0 * NWARP + wb) * R * 32 + iv) * 16;
+      const unsigned char* bd = smem_stage + ((size_t)(1 * NWARP + wb) * R * 32 + iv) * 16;
+      S.gz_t = Lay<Tl>::load_scalar(bt, lx % EPV);
+      S.gz_d = Lay<Tl>::load_scalar(bd, lx % EPV);
+    }
+    __syncwarp();
+    bool last = false;
+    if (lane == 0) last = stage_release_last(&S.cnt);
+    last = __shfl_sync(FULL, last, 0);
+    if (last && tma_next) issue_unit_load<Tl, R>(P, g, next_u, bar, smem_stage);
+  } else {
+    const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0) * ES;
+    const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0) * ES;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int v = g.vbeg + j * 32 + lane;
+      rt[j] = load_vec_direct<Tl>(tb, v, g.slen, v < g.vend);
+      if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen, v < g.vend);
+    }
+    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0 && (long long)x < g.slice0 + g.slen;
+    if (PAIR && tid == 0 && own_x) {
+      S.gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
+      S.gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
+    }
+  }
+
+  const bool t_ok = T >= 0.0f && T <= 3.0e38f;   // false for NaN and inf
+  const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
+  const bool x_ok = !PAIR || P.tv_only || (x >= 0 && x < V);
+  const float c = greedy ? 0.0f : fminf(__fdiv_rn(LOG2E_F, T), 3.0e38f);
+
+  // ---------------- pass A: per-warp statistics, pushed to every CTA of the cluster
+  MaxAcc<Tl> mx_t, mx_d;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    mx_t.add(rt[j]);
+    if (PAIR) mx_d.add(rd[j]);
+  }
+  X1 mine;
+  mine.m_t = warp_max_nan(mx_t.get());
+  mine.m_d = PAIR ? warp_max_nan(mx_d.get()) : -INFINITY;
+  mine.i_t = 0x7fffffff; mine.i_d = 0x7fffffff;
+  mine.s_t = 0.0f; mine.s_d = 0.0f;
+  mine.pad0 = 0; mine.pad1 = 0;
+  if (greedy) {
+    int ci_t = 0x7fffffff, ci_d = 0x7fffffff;   // lowest global index holding the warp maximum
+#pragma unroll
+    for (int j = R - 1; j >= 0; --j) {
+#pragma unroll
+      for (int e = EPV - 1; e >= 0; --e) {
+        const int gi = (int)g.slice0 + (g.vbeg + j * 32 + lane) * EPV + e;
+        if (Lay<Tl>::elem(rt[j], e) == mine.m_t) ci_t = gi;
+        if (PAIR && Lay<Tl>::elem(rd[j], e) == mine.m_d) ci_d = gi;
+      }
+    }
+    mine.i_t = (int)warp_min_u32((unsigned)ci_t);
+    if (PAIR) mine.i_d = (int)warp_min_u32((unsigned)ci_d);
+  } else {
+    const u64 cc = pk(c, c);
+    const float rwt = ref_of(mine.m_t, c);
+    mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
+    if (PAIR) {
+      const float rwd = ref_of(mine.m_d, c);
+      mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+    }
+  }
+  const int set1 = n1 & 1;
+  const uint32_t xbar = saddr(&S.xbar[set1]);
+  if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items * 32u);
+  if (lane < (int)g.C)
+    st_async_x1(peer_addr(saddr(&S.x1[set1][g.rank * NWARP + warp]), lane), mine, peer_addr(xbar, lane));
+  mbar_wait_cluster_bounded(xbar, (unsigned)((n1 >> 1) & 1), P.flags);
+  ++n1;
+
+  // Cluster merge, identical in every warp: lane l holds items l and l + 32.
+  X1 ia, ib;
+  {
+    X1 z;
+    z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
+    z.pad0 = 0; z.pad1 = 0;
+    ia = lane < g.items ? S.x1[set1][lane] : z;
+    ib = lane + 32 < g.items ? S.x1[set1][lane + 32] : z;
+  }
+  const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+  const float M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
+  int A_t = 0, A_d = 0;
+  float S_t = 0.0f, S_d = 0.0f, R_t = 0.0f, R_d = 0.0f;
+  if (greedy) {
+    A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
+    if (PAIR)
+      A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
+  } else {
+    R_t = ref_of(M_t, c);
+    S_t = warp_sum_f32(ia.s_t * pow2_int(ref_of(ia.m_t, c) - R_t) + ib.s_t * pow2_int(ref_of(ib.m_t, c) - R_t));
+    if (PAIR) {
+      R_d = ref_of(M_d, c);
+      S_d = warp_sum_f32(ia.s_d * pow2_int(ref_of(ia.m_d, c) - R_d) + ib.s_d * pow2_int(ref_of(ib.m_d, c) - R_d));
+    }
+  }
+  bool row_ok = isfinite(M_t) && (!PAIR || isfinite(M_d));
+  if (!greedy) {
+    row_ok = row_ok && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
+    if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
+  }
+  const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
+  const size_t ui = (size_t)b * (k + 1) + ipos;   // unit index within [B, k+1]
+  const size_t pi = (size_t)b * k + ipos;         // position index within [B, k]
+  const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
+
+  if (g.rank == 0 && tid == 0) {
+    UnitStat st;
+    st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
+    st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
+    P.ws_stat[ui] = st;
+    if (status != 0 || greedy) {
+      if (!P.tv_only && status == 0) {
+        P.ws_y[ui] = A_t;
+        if (PAIR) {
+          P.ws_acc[pi] = x == A_t;
+          if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
+          if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
+        }
+      }
+      if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
+    }
+  }
+  if (status != 0 || greedy) return;   // cluster-uniform
+  if (lane == 0)   // this range's part of S_t (for a draw from p when the residual is zero)
+    P.ws_p[ui * ITEMS_MAX + g.rank * NWARP + warp] = mine.s_t * pow2_int(ref_of(mine.m_t, c) - R_t);
+
+  // ---------------- pass B: residual (pair) or target (bonus) mass of this warp's range
+  const u64 cc = pk(c, c);
+  const u64 nrt = pk(-R_t, -R_t), nrd = pk(-R_d, -R_d);
+  const u64 nr = pk(-r_f, -r_f);
+  float w0 = 0.0f, w1 = 0.0f;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const float wj = vec_weight_sum<Tl, PAIR>(rt[j], rd[PAIR ? j : 0], cc, nrt, nrd, nr);
+    if (j & 1) w1 += wj; else w0 += wj;
+  }
+  const float wwarp = warp_sum_f32(w0 + w1);
+  if (lane == 0) P.ws_w[ui * ITEMS_MAX + g.rank * NWARP + warp] = wwarp;
+  if (PAIR && own_x && tid == 0) {   // accept test at the drafted token
+    const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
+    const float ratio = exp2f(lpx - lqx) * (S_d / S_t);
+    const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
+    P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
+    if (P.out_p) P.out_p[pi] = exp2f(lpx) / S_t;
+    if (P.out_q) P.out_q[pi] = exp2f(lqx) / S_d;
+  }
+}
+
+template <typename Tl, int R>
+__global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   Small& S = *reinterpret_cast<Small*>(smem);
-  const uint4* stage_t = reinterpret_cast<const uint4*>(smem + SMALL_BYTES);
-  const uint4* stage_d = reinterpret_cast<const uint4*>(smem + SMALL_BYTES + (size_t)P.Vs * ES);
+  unsigned char* stage = smem + SMALL_BYTES;   // [2 rows][NWARP][R*32] vectors
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned C = cl_size(), rank = cl_rank();
+  const int tid = threadIdx.x, warp = tid >> 5;
+  Geo g;
+  g.C = cl_size();
+  g.rank = cl_rank();
+  g.items = (int)g.C * NWARP;
+  g.slice0 = (long long)g.rank * P.Vs;
+  g.slen = (int)max(0LL, min((long long)P.Vs, (long long)P.V - g.slice0));
+  g.nvec = (g.slen + Lay<Tl>::EPV - 1) / Lay<Tl>::EPV;
+  g.vbeg = warp * P.wv;
+  g.vend = min(g.vbeg + P.wv, g.nvec);
   const unsigned cid = cl_id(), ncl = cl_count();
-  const int k = P.k, V = P.V, upc = P.units_per_chain;
-  const int items = (int)C * NWARP;
-  const long long slice0 = (long long)rank * P.Vs;
-  const int slen = (int)max(0LL, min((long long)P.Vs, (long long)V - slice0));
-  const int nvec = (slen + EPV - 1) / EPV;
-  const int vbeg = warp * P.wv;
-  const int vend = min(vbeg + P.wv, nvec);
+  const int upc = P.units_per_chain, k = P.k;
   const long long n_units = (long long)P.B * upc;
   const uint32_t bar = saddr(&S.bar);
-  const uint32_t stage_t_s = saddr(stage_t), stage_d_s = saddr(stage_d);
+  const uint4* blk_t = reinterpret_cast<const uint4*>(stage) + (size_t)(0 * NWARP + warp) * R * 32;
+  const uint4* blk_d = reinterpret_cast<const uint4*>(stage) + (size_t)(1 * NWARP + warp) * R * 32;
 
+  if (P.tma) {   // the tails of the warp blocks stay -inf for the whole kernel
+    uint4* st = reinterpret_cast<uint4*>(stage);
+    for (int i = tid; i < 2 * NWARP * R * 32; i += NT) st[i] = Lay<Tl>::neg_inf();
+  }
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(saddr(&S.xbar[0]), 1);
+    mbar_init(saddr(&S.xbar[1]), 1);
     S.cnt = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   cluster_sync_all();   // every peer's shared memory is live before the first remote store
 
-  auto unit_rows = [&](long long u, long long& trow, long long& drow, int& ipos, int& b, bool& pair) {
-    b = (int)(u / upc);
-    ipos = (int)(u % upc);
-    pair = ipos < k;
-    trow = (long long)b * (k + 1) + ipos;
-    drow = (long long)b * k + ipos;
-  };
-  auto issue_load = [&](long long u) {   // one thread
-    long long trow, drow; int ipos, b; bool pair;
-    unit_rows(u, trow, drow, ipos, b, pair);
-    if (slen > 0) {
-      const unsigned bytes = (unsigned)slen * ES;
-      mbar_expect_tx(bar, pair ? 2 * bytes : bytes);
-      bulk_g2s(stage_t_s, (const char*)P.target + ((size_t)trow * V + slice0) * ES, bytes, bar);
-      if (pair) bulk_g2s(stage_d_s, (const char*)P.draft + ((size_t)drow * V + slice0) * ES, bytes, bar);
-    } else {
-      mbar_arrive(bar);
-    }
-  };
-
   long long u = cid;
-  if (P.tma && tid == 0 && u < n_units) issue_load(u);
+  if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, u, bar, stage);
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
-
   for (; u < n_units; u += ncl, phase ^= 1u) {
-    long long trow, drow; int ipos, b; bool pair;
-    unit_rows(u, trow, drow, ipos, b, pair);
-
-    // ---------------- per-chain scalars (identical in every CTA of the cluster)
-    const float T = P.temperature[b];
-    const int x = pair && !P.tv_only ? P.tokens[(size_t)b * k + ipos] : 0;
-    const bool t_ok = T >= 0.0f && T <= 3.0e38f;   // false for NaN and inf
-    const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
-    const bool x_ok = !pair || P.tv_only || (x >= 0 && x < V);
-    const bool own_x = pair && !P.tv_only && x_ok && (long long)x >= slice0 && (long long)x < slice0 + slen;
-
-    // ---------------- this warp's vectors of the unit into registers
-    uint4 rt[R], rd[R];
-    float gz_t = 0.0f, gz_d = 0.0f;   // logits at the drafted token (thread 0 of its owner CTA)
-    if (P.tma) {
-      mbar_wait_bounded(bar, phase, P.flags);
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int v = vbeg + j * 32 + lane;
-        rt[j] = v < vend ? stage_t[v] : Lay<Tl>::neg_inf();
-        rd[j] = (pair && v < vend) ? stage_d[v] : Lay<Tl>::neg_inf();
-      }
-      if (tid == 0 && own_x) {
-        gz_t = Lay<Tl>::load_scalar(stage_t, x - slice0);
-        gz_d = Lay<Tl>::load_scalar(stage_d, x - slice0);
-      }
-      __syncwarp();
-      if (lane == 0 && stage_release_last(&S.cnt) && u + ncl < n_units) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue_load(u + ncl);
-      }
-    } else {
-      const char* tb = (const char*)P.target + ((size_t)trow * V + slice0) * ES;
-      const char* db = (const char*)P.draft + ((size_t)drow * V + slice0) * ES;
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int v = vbeg + j * 32 + lane;
-        rt[j] = load_vec_direct<Tl>(tb, v, slen, v < vend);
-        rd[j] = load_vec_direct<Tl>(db, v, slen, pair && v < vend);
-      }
-      if (tid == 0 && own_x) {
-        gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
-        gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
-      }
-    }
-
-    const float c = greedy ? 0.0f : fminf(__fdiv_rn(LOG2E_F, T), 3.0e38f);
-
-    // ---------------- pass A: per-warp statistics, pushed to every CTA of the cluster
-    float tm_t = -INFINITY, tm_d = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      tm_t = nanmax(tm_t, vec_max<Tl>(rt[j]));
-      if (pair) tm_d = nanmax(tm_d, vec_max<Tl>(rd[j]));
-    }
-    X1 mine;
-    mine.m_t = warp_max_nan(tm_t);
-    mine.m_d = pair ? warp_max_nan(tm_d) : -INFINITY;
-    mine.i_t = 0x7fffffff; mine.i_d = 0x7fffffff;
-    mine.s_t = 0.0f; mine.s_d = 0.0f;
-    mine.pad0 = 0; mine.pad1 = 0;
-    if (greedy) {
-      int ci_t = 0x7fffffff, ci_d = 0x7fffffff;   // lowest global index holding the warp maximum
-#pragma unroll
-      for (int j = R - 1; j >= 0; --j) {
-#pragma unroll
-        for (int e = EPV - 1; e >= 0; --e) {
-          const int gi = (int)slice0 + (vbeg + j * 32 + lane) * EPV + e;
-          if (Lay<Tl>::elem(rt[j], e) == mine.m_t) ci_t = gi;
-          if (pair && Lay<Tl>::elem(rd[j], e) == mine.m_d) ci_d = gi;
-        }
-      }
-      mine.i_t = (int)warp_min_u32((unsigned)ci_t);
-      mine.i_d = (int)warp_min_u32((unsigned)ci_d);
-    } else {
-      const u64 cc = pk(c, c);
-      const float rwt = ref_of(mine.m_t, c), rwd = ref_of(mine.m_d, c);
-      const u64 nrt = pk(-rwt, -rwt), nrd = pk(-rwd, -rwd);
-      u64 at = 0ull, ad = 0ull;
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        at = add2(at, vec_expsum<Tl>(rt[j], cc, nrt));
-        if (pair) ad = add2(ad, vec_expsum<Tl>(rd[j], cc, nrd));
-      }
-      float lo, hi;
-      upk(at, lo, hi);
-      mine.s_t = warp_sum_f32(lo + hi);
-      upk(ad, lo, hi);
-      mine.s_d = pair ? warp_sum_f32(lo + hi) : 0.0f;
-    }
-    const int set1 = n1 & 1;
-    if (lane < (int)C) st_peer_x1(peer_addr(saddr(&S.x1[set1][rank * NWARP + warp]), lane), mine);
-    cluster_sync_all();
-    ++n1;
-
-    // Cluster merge, identical in every warp: lane l holds items l and l + 32.
-    X1 ia, ib;
-    {
-      X1 z;
-      z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
-      z.pad0 = 0; z.pad1 = 0;
-      ia = lane < items ? S.x1[set1][lane] : z;
-      ib = lane + 32 < items ? S.x1[set1][lane + 32] : z;
-    }
-    const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
-    const float M_d = warp_max_nan(nanmax(ia.m_d, ib.m_d));
-    int A_t = 0, A_d = 0;
-    float S_t = 0.0f, S_d = 0.0f, R_t = 0.0f, R_d = 0.0f;
-    if (greedy) {
-      A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
-      A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
-    } else {
-      R_t = ref_of(M_t, c);
-      R_d = ref_of(M_d, c);
-      S_t = warp_sum_f32(ia.s_t * pow2_int(ref_of(ia.m_t, c) - R_t) + ib.s_t * pow2_int(ref_of(ib.m_t, c) - R_t));
-      S_d = warp_sum_f32(ia.s_d * pow2_int(ref_of(ia.m_d, c) - R_d) + ib.s_d * pow2_int(ref_of(ib.m_d, c) - R_d));
-    }
-    bool row_ok = isfinite(M_t) && (!pair || isfinite(M_d));
-    if (!greedy) {
-      row_ok = row_ok && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
-      if (pair) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
-    }
-    const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
-    const size_t ui = (size_t)b * (k + 1) + ipos;   // unit index within [B, k+1]
-    const size_t pi = (size_t)b * k + ipos;         // position index within [B, k]
-    const float r_f = pair && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
-
-    if (rank == 0 && tid == 0) {
-      UnitStat st;
-      st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
-      st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
-      P.ws_stat[ui] = st;
-      if (status != 0 || greedy) {
-        if (!P.tv_only && status == 0) {
-          P.ws_y[ui] = A_t;
-          if (pair) {
-            P.ws_acc[pi] = x == A_t;
-            if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
-            if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
-          }
-        }
-        if (pair && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
-      }
-    }
-    if (status != 0 || greedy) continue;   // cluster-uniform
-
-    // ---------------- pass B: residual (pair) or target (bonus) mass of this warp's range
-    const u64 cc = pk(c, c);
-    const u64 nrt = pk(-R_t, -R_t), nrd = pk(-R_d, -R_d);
-    const u64 nr = pk(-r_f, -r_f);
-    float wthr = 0.0f;
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-      wthr += pair ? vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr)
-                   : vec_weight_sum<Tl, false>(rt[j], rd[j], cc, nrt, nrd, nr);
-    }
-    const float wwarp = warp_sum_f32(wthr);
-    if (lane == 0) {
-      const size_t it = ui * ITEMS_MAX + rank * NWARP + warp;
-      P.ws_w[it] = wwarp;
-      P.ws_p[it] = mine.s_t * pow2_int(ref_of(mine.m_t, c) - R_t);   // this range's part of S_t
-    }
-    if (own_x && tid == 0) {   // accept test at the drafted token
-      const float lpx = fmaf(gz_t, c, -R_t), lqx = fmaf(gz_d, c, -R_d);
-      const float ratio = exp2f(lpx - lqx) * (S_d / S_t);
-      const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
-      P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
-      if (P.out_p) P.out_p[pi] = exp2f(lpx) / S_t;
-      if (P.out_q) P.out_q[pi] = exp2f(lqx) / S_d;
-    }
+    const int b = (int)(u / upc), ipos = (int)(u % upc);
+    const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
+    const bool tma_next = P.tma && u + ncl < n_units;
+    if (ipos < k)
+      process_unit<Tl, R, true>(P, S, blk_t, blk_d, g, u, b, ipos, trow, drow, phase, n1, bar, stage, u + ncl, tma_next);
+    else
+      process_unit<Tl, R, false>(P, S, blk_t, blk_d, g, u, b, ipos, trow, drow, phase, n1, bar, stage, u + ncl, tma_next);
   }
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
 }
@@ -885,7 +1002,7 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   h->max_batch = max_batch; h->k = k; h->V = vocab; h->dtype = logit_dtype; h->flags = flags;
   h->C = C; h->Vs = (int)Vs; h->R = R; h->wv = (int)wv;
   h->tma_ok = ((size_t)vocab * es) % 16 == 0 && !(flags & SV_FLAG_NO_TMA);
-  h->smem = SMALL_BYTES + 2 * (size_t)Vs * es;
+  h->smem = SMALL_BYTES + (h->tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
   if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->finalize);
   else pick_kernels<__nv_bfloat16>(R, h->kernel, h->finalize);
   if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
