@@ -108,6 +108,35 @@ int spec_verify(spec_verify_t h, int batch,
                 float* out_p_draft, float* out_q_draft, float* out_tv,
                 void* cuda_stream);
 
+/* Allocation-free spec_verify.  The pages have no counterpart of this call;
+ * it exists for callers that cannot allocate device memory.  cudaMalloc may
+ * synchronise the whole device, and a serving engine that has reserved its
+ * memory for the KV cache at start-up may refuse any further allocation, so
+ * such callers cannot use spec_verify_init.  This call takes no handle and
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine):
+ * its workspace is a file-scope device array of SV_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading the library holds until the process exits.
+ * Arguments, layouts, outputs and invalid-chain reporting (tau = -1) are
+ * those of spec_verify, plus k, vocab and logit_dtype in place of a handle.
+ * Limit: the workspace needs about 4*k + 548*(k+1) bytes per chain (4,412 at
+ * k = 7), so batch may be up to about 1,900 chains at k = 7 and 950 at
+ * k = 15; larger batches return SV_ERR_SIZE before any launch.
+ * Notes: the first call on each device does a one-time set-up (looks up the
+ * array's device address with cudaGetSymbolAddress, sets kernel attributes,
+ * queries occupancy) and should be made before any stream capture.  All
+ * calls share the one array and its contents persist between calls (the
+ * counters that must start at zero are cleared on the stream at each call),
+ * so calls that overlap on the GPU, on different streams, race with each
+ * other: order them on one stream.  Data and timeout counters of this call
+ * are not reported; invalid chains show up as tau = -1. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype,
+                        const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                        int32_t* out_tokens, int32_t* out_tau,
+                        float* out_p_draft, float* out_q_draft, float* out_tv,
+                        void* cuda_stream);
+
 /* Per-position TV distance only: out_tv[b, i] = 0.5 * sum_j |p_{i+1}(j) - q_{i+1}(j)|
  * for the k target/draft row pairs of each chain (the target's bonus row is
  * not read).  A position whose rows or temperature are invalid gets NaN.

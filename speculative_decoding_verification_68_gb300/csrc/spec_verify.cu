@@ -37,6 +37,8 @@
 #include <string.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "spec_verify.h"
 
 namespace {
@@ -957,6 +959,116 @@ static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* 
   return SV_OK;
 }
 
+// ---------------------------------------------------- allocation-free entry
+// spec_verify_noalloc keeps its workspace in this file-scope device array
+// instead of memory from cudaMalloc.  Every GPU that loads the library holds
+// one copy until the process exits.  Host code must not use the array's name
+// as a device address: the address is looked up once per device with
+// cudaGetSymbolAddress and passed to the kernels.
+constexpr size_t NOALLOC_BYTES = (size_t)SV_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+namespace {
+struct NoallocDevice {       // per-device set-up, done by the first call on that device
+  bool ready;
+  unsigned char* scratch;    // device address of g_noalloc_scratch
+};
+constexpr int NOALLOC_MAX_DEVICES = 64;
+NoallocDevice g_noalloc_dev[NOALLOC_MAX_DEVICES];
+struct NoallocPlan {         // launch geometry cached per (device, k, V, dtype)
+  bool used;
+  int device, k, V, dtype;
+  spec_verify_ctx plan;      // only the geometry and kernel fields are filled
+};
+constexpr int NOALLOC_PLANS = 32;
+NoallocPlan g_noalloc_plans[NOALLOC_PLANS];
+std::mutex g_noalloc_lock;
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Byte offsets of the workspace arrays inside the scratch array.
+struct NoallocLayout {
+  size_t flags, acc, y, stat, w, p, total;
+};
+NoallocLayout noalloc_layout(size_t B, size_t k) {
+  NoallocLayout L;
+  L.flags = 0;
+  L.acc = align256(L.flags + 4 * sizeof(int));
+  L.y = align256(L.acc + B * k * sizeof(int32_t));
+  L.stat = align256(L.y + B * (k + 1) * sizeof(int32_t));
+  L.w = align256(L.stat + B * (k + 1) * sizeof(UnitStat));
+  L.p = align256(L.w + B * (k + 1) * ITEMS_MAX * sizeof(float));
+  L.total = L.p + B * (k + 1) * ITEMS_MAX * sizeof(float);
+  return L;
+}
+
+// Geometry, kernels and occupancy for (k, V, dtype) on the current device;
+// the same choices spec_verify_init makes.  Allocates nothing.
+int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) {
+  for (int i = 0; i < NOALLOC_PLANS; ++i) {
+    const NoallocPlan& c = g_noalloc_plans[i];
+    if (c.used && c.device == device && c.k == k && c.V == vocab && c.dtype == dtype) {
+      out = c.plan;
+      return SV_OK;
+    }
+  }
+  spec_verify_ctx h;
+  memset(&h, 0, sizeof h);
+  const int es = dtype == SV_FP32 ? 4 : 2;
+  const int epv = 16 / es;
+  int C = 1;
+  for (int c = CMAX; c >= 1; c >>= 1) {
+    const long long vs = ((long long)(vocab + c - 1) / c + epv - 1) / epv * epv;
+    if (vs >= (long long)NT * epv || c == 1) { C = c; break; }
+  }
+  const long long Vs = ((long long)(vocab + C - 1) / C + epv - 1) / epv * epv;
+  const long long nvec = Vs / epv;
+  const long long wv = (nvec + NWARP - 1) / NWARP;
+  const long long r_need = (wv + 31) / 32;
+  int R = -1;
+  for (int i = 0; i < N_R; ++i)
+    if (R_CHOICES[i] >= r_need) { R = R_CHOICES[i]; break; }
+  if (R < 0) return SV_ERR_SIZE;
+  h.device = device; h.k = k; h.V = vocab; h.dtype = dtype;
+  h.C = C; h.Vs = (int)Vs; h.R = R; h.wv = (int)wv;
+  h.tma_ok = ((size_t)vocab * es) % 16 == 0;
+  h.smem = SMALL_BYTES + (h.tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
+  if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.finalize);
+  else pick_kernels<__nv_bfloat16>(R, h.kernel, h.finalize);
+  if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem) != cudaSuccess)
+    return SV_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = h.smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, h.kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  h.n_clusters = n;
+  for (int i = 0; i < NOALLOC_PLANS; ++i) {
+    if (!g_noalloc_plans[i].used) {
+      g_noalloc_plans[i].used = true;
+      g_noalloc_plans[i].device = device; g_noalloc_plans[i].k = k; g_noalloc_plans[i].V = vocab;
+      g_noalloc_plans[i].dtype = dtype;
+      g_noalloc_plans[i].plan = h;
+      break;
+    }
+  }
+  out = h;
+  return SV_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* spec_verify_strerror(int code) {
@@ -1098,6 +1210,62 @@ int spec_verify(spec_verify_t h, int batch, const void* target_logits, const voi
   int rc = launch_fused(h, P, (long long)batch * (h->k + 1), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s);
+}
+
+int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype, const void* target_logits,
+                        const void* draft_logits, const int32_t* draft_tokens, const float* temperature,
+                        const float* uniforms, int32_t* out_tokens, int32_t* out_tau, float* out_p_draft,
+                        float* out_q_draft, float* out_tv, void* cuda_stream) {
+  if (batch < 0) return SV_ERR_ARG;
+  if (logit_dtype != SV_FP32 && logit_dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (k < 1 || k > 31 || vocab < 1) return SV_ERR_SIZE;
+  const NoallocLayout L = noalloc_layout((size_t)batch, (size_t)k);
+  if (L.total > NOALLOC_BYTES) return SV_ERR_SIZE;
+  if (batch == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !temperature || !uniforms || !out_tokens || !out_tau)
+    return SV_ERR_ARG;
+  const int es = logit_dtype == SV_FP32 ? 4 : 2;
+  if (((uintptr_t)target_logits % es) || ((uintptr_t)draft_logits % es)) return SV_ERR_ARG;
+  if (!al4(draft_tokens) || !al4(temperature) || !al4(uniforms) || !al4(out_tokens) || !al4(out_tau) ||
+      !al4(out_p_draft) || !al4(out_q_draft) || !al4(out_tv))
+    return SV_ERR_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return SV_ERR_CUDA;
+  if (device < 0 || device >= NOALLOC_MAX_DEVICES) return SV_ERR_ARG;
+  spec_verify_ctx h;
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> guard(g_noalloc_lock);
+    NoallocDevice& d = g_noalloc_dev[device];
+    if (!d.ready) {   // once per device, with that device current
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+      }
+      d.scratch = (unsigned char*)ptr;
+      d.ready = true;
+    }
+    scratch = d.scratch;
+    const int rc = noalloc_plan(device, k, vocab, logit_dtype, h);
+    if (rc != SV_OK) return rc;
+  }
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  int* flags = (int*)(scratch + L.flags);
+  if (cudaMemsetAsync(flags, 0, 4 * sizeof(int), s) != cudaSuccess) return SV_ERR_CUDA;   // counters start at zero
+  KParams P;
+  memset(&P, 0, sizeof P);
+  P.target = target_logits; P.draft = draft_logits; P.tokens = draft_tokens; P.temperature = temperature;
+  P.uniforms = uniforms; P.out_p = out_p_draft; P.out_q = out_q_draft; P.out_tv = out_tv;
+  P.ws_acc = (int32_t*)(scratch + L.acc); P.ws_y = (int32_t*)(scratch + L.y);
+  P.ws_stat = (UnitStat*)(scratch + L.stat); P.ws_w = (float*)(scratch + L.w); P.ws_p = (float*)(scratch + L.p);
+  P.flags = flags;
+  P.B = batch; P.k = k; P.V = vocab; P.Vs = h.Vs; P.wv = h.wv;
+  P.units_per_chain = k + 1; P.tv_only = 0;
+  P.tma = h.tma_ok && al16(target_logits) && al16(draft_logits);
+  int rc = launch_fused(&h, P, (long long)batch * (k + 1), s);
+  if (rc != SV_OK) return rc;
+  return launch_finalize(&h, P, draft_tokens, out_tokens, out_tau, s);
 }
 
 int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
