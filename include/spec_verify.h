@@ -82,7 +82,8 @@ enum {
  * decisions, greedy tokens, row statistics and per-range masses: about
  * 552*(k+1) bytes per chain) and, with SV_FLAG_HOST_STAGING, device copies of
  * every input and output for max_batch chains.  Uses the current CUDA device; the handle
- * must be used on that device.  Writes NULL to *h on failure. */
+ * must be used on that device.  SV_ERR_SIZE also when max_batch*(k+1) reaches
+ * 2^31.  Writes NULL to *h on failure. */
 int spec_verify_init(spec_verify_t* h, int max_batch, int k, int vocab, int logit_dtype, unsigned flags);
 
 /* Verify `batch` chains (0 <= batch <= max_batch).

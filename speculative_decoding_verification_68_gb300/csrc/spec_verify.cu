@@ -91,9 +91,20 @@ struct KParams {
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
   float m_t, m_d;              // maxima of the warp's range in the target / draft row
-  float s_t, s_d;              // sums of 2^(z*c - ref(m)) over the range
+  float s_t, s_d;              // sums of 2^(z*c - ref) over the range
   int i_t, i_d;                // lowest index of the maximum (T == 0)
-  int pad0, pad1;
+  int ref_t, ref_d;            // the integer references ceil(m*c) (NO_REF for an empty range)
+};
+constexpr int NO_REF = -0x7fffffff - 1;
+
+// Row statistics of one unit, merged by warp 0 of each CTA and read by the others.
+struct alignas(16) Merged {
+  float S_t, S_d;      // sums of 2^(z*c - R) over the whole rows
+  float R_t, R_d;      // integer references of the rows
+  float r;             // S_t / S_d
+  int IR_t;            // R_t as an integer (NO_REF if the row has no finite maximum)
+  int status;          // ST_* bits, 0 if valid
+  int pad;
 };
 
 struct Small {
@@ -103,6 +114,7 @@ struct Small {
   float gz_t, gz_d;            // logits at the drafted token (thread 0 of the owner CTA)
   int pad0;
   X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
+  Merged mg[2];                // merged row statistics (warp 0 to the other warps), per slot set
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "bookkeeping area too small");
 
@@ -121,11 +133,6 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t a, unsigned rank) {
   return r;
 }
 
-__device__ __forceinline__ void st_peer_x1(uint32_t a, const X1& v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(__float_as_uint(v.m_t)),
-               "r"(__float_as_uint(v.m_d)), "r"(__float_as_uint(v.s_t)), "r"(__float_as_uint(v.s_d)) : "memory");
-  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a + 16), "r"(v.i_t), "r"(v.i_d) : "memory");
-}
 // Asynchronous remote store of one exchange part; completes its 32 bytes on
 // the receiver's mbarrier (no fence or barrier on the sender's side).
 __device__ __forceinline__ void st_async_x1(uint32_t slot, const X1& v, uint32_t rbar) {
@@ -133,7 +140,7 @@ __device__ __forceinline__ void st_async_x1(uint32_t slot, const X1& v, uint32_t
                ::"r"(slot), "r"(__float_as_uint(v.m_t)), "r"(__float_as_uint(v.m_d)), "r"(__float_as_uint(v.s_t)),
                "r"(__float_as_uint(v.s_d)), "r"(rbar) : "memory");
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-               ::"r"(slot + 16), "r"(v.i_t), "r"(v.i_d), "r"(v.pad0), "r"(v.pad1), "r"(rbar) : "memory");
+               ::"r"(slot + 16), "r"(v.i_t), "r"(v.i_d), "r"(v.ref_t), "r"(v.ref_d), "r"(rbar) : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) { asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory"); }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
@@ -172,11 +179,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, unsigned
 __device__ __forceinline__ float ex2(float x) { float y; asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x)); return y; }
 __device__ __forceinline__ float nanmax(float a, float b) { float y; asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b)); return y; }
 __device__ __forceinline__ float warp_max_nan(float v) { float y; asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(v)); return y; }
-// 2^n for an integer-valued n <= 0, exact (0 below the normal range)
-__device__ __forceinline__ float pow2_int(float n) {
-  const int e = (int)n;
-  return e < -126 ? 0.0f : __int_as_float((e + 127) << 23);
-}
 __device__ __forceinline__ unsigned warp_min_u32(unsigned v) { unsigned y; asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(y) : "r"(v)); return y; }
 typedef unsigned long long u64;
 __device__ __forceinline__ u64 pk(float lo, float hi) { u64 r; asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi)); return r; }
@@ -191,11 +193,18 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
   return v;
 }
-// integer log2-domain reference for a row maximum m (0 for an empty/invalid part)
-__device__ __forceinline__ float ref_of(float m, float c) {
-  float r = ceilf(m * c);
-  return (isfinite(m) && isfinite(r)) ? r : 0.0f;
+// Integer log2-domain reference ceil(m*c) of a range maximum m; NO_REF for a range
+// without a finite maximum (or beyond the supported range).
+__device__ __forceinline__ int iref_of(float m, float c) {
+  const float r = ceilf(m * c);
+  return (isfinite(m) && fabsf(r) < REF_LIMIT) ? (int)r : NO_REF;
 }
+// 2^(a - b) for integer references a <= b (exact; 0 below the normal range or for NO_REF)
+__device__ __forceinline__ float pow2_diff(int a, int b) {
+  const int d = a == NO_REF ? -1000 : a - b;
+  return d < -126 ? 0.0f : __int_as_float((d + 127) << 23);
+}
+__device__ __forceinline__ int warp_max_s32(int v) { int y; asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(y) : "r"(v)); return y; }
 
 // ------------------------------------------------------------ per-type access
 // Arrive on the stage counter; the last of NWARP warps returns true (acq_rel,
@@ -230,36 +239,6 @@ template <> struct Lay<__nv_bfloat16> {
     return __uint_as_float((uint32_t)((const uint16_t*)p)[i] << 16);
   }
 };
-
-template <typename Tl> __device__ __forceinline__ float vec_max(const uint4& v);
-template <> __device__ __forceinline__ float vec_max<float>(const uint4& v) {
-  return nanmax(nanmax(__uint_as_float(v.x), __uint_as_float(v.y)), nanmax(__uint_as_float(v.z), __uint_as_float(v.w)));
-}
-template <> __device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4& v) {
-  __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&v.x);
-  __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v.y);
-  __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&v.z);
-  __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&v.w);
-  __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
-  return nanmax(__low2float(m), __high2float(m));
-}
-
-// Sum over one vector of 2^(z*c + nref), as a packed pair accumulator.
-template <typename Tl> __device__ __forceinline__ u64 vec_expsum(const uint4& v, u64 cc, u64 nr);
-template <> __device__ __forceinline__ u64 vec_expsum<float>(const uint4& v, u64 cc, u64 nr) {
-  float a0, a1, a2, a3;
-  upk(fma2(pk(__uint_as_float(v.x), __uint_as_float(v.y)), cc, nr), a0, a1);
-  upk(fma2(pk(__uint_as_float(v.z), __uint_as_float(v.w)), cc, nr), a2, a3);
-  return add2(pk(ex2(a0), ex2(a1)), pk(ex2(a2), ex2(a3)));
-}
-template <> __device__ __forceinline__ u64 vec_expsum<__nv_bfloat16>(const uint4& v, u64 cc, u64 nr) {
-  float a0, a1, a2, a3, a4, a5, a6, a7;
-  upk(fma2(pk(bf_lo(v.x), bf_hi(v.x)), cc, nr), a0, a1);
-  upk(fma2(pk(bf_lo(v.y), bf_hi(v.y)), cc, nr), a2, a3);
-  upk(fma2(pk(bf_lo(v.z), bf_hi(v.z)), cc, nr), a4, a5);
-  upk(fma2(pk(bf_lo(v.w), bf_hi(v.w)), cc, nr), a6, a7);
-  return add2(add2(pk(ex2(a0), ex2(a1)), pk(ex2(a2), ex2(a3))), add2(pk(ex2(a4), ex2(a5)), pk(ex2(a6), ex2(a7))));
-}
 
 // Unscaled residual weights of one pair of elements: max(0, e_t - r * e_d)
 // with e = 2^(z*c - R) and r = S_t / S_d, i.e. S_t * max(0, p - q).  One
@@ -402,19 +381,32 @@ struct Geo {
   int slen, nvec, vbeg, vend;
 };
 
+// Units are taken position-major, u = ipos * B + b, so that every cluster's
+// walk u = cluster_id, cluster_id + n_clusters, ... meets every position
+// (and the cheaper bonus rows) equally often.
+struct Unit {
+  int b, ipos;
+};
+__device__ __forceinline__ Unit unit_of(unsigned u, unsigned B) {
+  const unsigned ipos = u / B;
+  Unit r;
+  r.b = (int)(u - ipos * B);
+  r.ipos = (int)ipos;
+  return r;
+}
+
 // Bulk copies of one unit into the warp blocks of the stage, issued by one
 // whole warp: lane 0 arms the mbarrier with the byte count, then lane w
 // copies warp w's range of the target row and lane 8 + w that of the draft row.
 template <typename Tl, int R>
-__device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, long long u, uint32_t bar,
+__device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, Unit n, uint32_t bar,
                                                 const unsigned char* stage) {
   constexpr int ES = (int)sizeof(Tl);
   const int lane = threadIdx.x & 31;
-  const int upc = P.units_per_chain, k = P.k;
-  const int b = (int)(u / upc), ipos = (int)(u % upc);
-  const bool pair = ipos < k;
+  const int k = P.k;
+  const bool pair = n.ipos < k;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic accesses of the stage first
-  const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
+  const long long trow = (long long)n.b * (k + 1) + n.ipos, drow = (long long)n.b * k + n.ipos;
   if (lane == 0) {
     const unsigned bytes = (unsigned)g.nvec * 16u;
     if (bytes > 0) mbar_expect_tx(bar, pair ? 2 * bytes : bytes);
@@ -434,19 +426,20 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
   }
 }
 
+// Named barrier 1 over the whole CTA: warp 0 publishes the merged statistics.
+__device__ __forceinline__ void merged_arrive() { asm volatile("bar.arrive 1, %0;" ::"n"(NT) : "memory"); }
+__device__ __forceinline__ void merged_wait() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+
 template <typename Tl, int R, bool PAIR>
 __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
-                                             const Geo& g, long long u, int b, int ipos, long long trow,
-                                             long long drow, unsigned phase, int& n1, const uint32_t bar,
-                                             const unsigned char* smem_stage, long long next_u, bool tma_next) {
+                                             const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
+                                             const unsigned char* smem_stage, const Unit next, bool tma_next,
+                                             const float T, const int x) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, V = P.V;
-
-  // per-chain scalars: issued before the stage wait so their latency overlaps it
-  const float T = P.temperature[b];
-  const int x = PAIR && !P.tv_only ? P.tokens[(size_t)b * k + ipos] : 0;
+  const int b = un.b, ipos = un.ipos;
 
   // ---------------- this warp's vectors of the unit into registers
   uint4 rt[R], rd[R];
@@ -471,8 +464,9 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     bool last = false;
     if (lane == 0) last = stage_release_last(&S.cnt);
     last = __shfl_sync(FULL, last, 0);
-    if (last && tma_next) issue_unit_load<Tl, R>(P, g, next_u, bar, smem_stage);
+    if (last && tma_next) issue_unit_load<Tl, R>(P, g, next, bar, smem_stage);
   } else {
+    const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
     const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0) * ES;
     const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0) * ES;
 #pragma unroll
@@ -505,7 +499,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   mine.m_d = PAIR ? warp_max_nan(mx_d.get()) : -INFINITY;
   mine.i_t = 0x7fffffff; mine.i_d = 0x7fffffff;
   mine.s_t = 0.0f; mine.s_d = 0.0f;
-  mine.pad0 = 0; mine.pad1 = 0;
+  mine.ref_t = NO_REF; mine.ref_d = NO_REF;
   if (greedy) {
     int ci_t = 0x7fffffff, ci_d = 0x7fffffff;   // lowest global index holding the warp maximum
 #pragma unroll
@@ -521,10 +515,12 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     if (PAIR) mine.i_d = (int)warp_min_u32((unsigned)ci_d);
   } else {
     const u64 cc = pk(c, c);
-    const float rwt = ref_of(mine.m_t, c);
+    mine.ref_t = iref_of(mine.m_t, c);
+    const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
     if (PAIR) {
-      const float rwd = ref_of(mine.m_d, c);
+      mine.ref_d = iref_of(mine.m_d, c);
+      const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
       mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
     }
   }
@@ -533,84 +529,114 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items * 32u);
   if (lane < (int)g.C)
     st_async_x1(peer_addr(saddr(&S.x1[set1][g.rank * NWARP + warp]), lane), mine, peer_addr(xbar, lane));
-  mbar_wait_cluster_bounded(xbar, (unsigned)((n1 >> 1) & 1), P.flags);
+  const unsigned xpar = (unsigned)((n1 >> 1) & 1);
   ++n1;
 
-  // Cluster merge, identical in every warp: lane l holds items l and l + 32.
-  X1 ia, ib;
-  {
-    X1 z;
-    z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
-    z.pad0 = 0; z.pad1 = 0;
-    ia = lane < g.items ? S.x1[set1][lane] : z;
-    ib = lane + 32 < g.items ? S.x1[set1][lane + 32] : z;
-  }
-  const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
-  const float M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
-  int A_t = 0, A_d = 0;
-  float S_t = 0.0f, S_d = 0.0f, R_t = 0.0f, R_d = 0.0f;
-  if (greedy) {
-    A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
-    if (PAIR)
-      A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
-  } else {
-    R_t = ref_of(M_t, c);
-    S_t = warp_sum_f32(ia.s_t * pow2_int(ref_of(ia.m_t, c) - R_t) + ib.s_t * pow2_int(ref_of(ib.m_t, c) - R_t));
-    if (PAIR) {
-      R_d = ref_of(M_d, c);
-      S_d = warp_sum_f32(ia.s_d * pow2_int(ref_of(ia.m_d, c) - R_d) + ib.s_d * pow2_int(ref_of(ib.m_d, c) - R_d));
-    }
-  }
-  bool row_ok = isfinite(M_t) && (!PAIR || isfinite(M_d));
-  if (!greedy) {
-    row_ok = row_ok && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
-    if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
-  }
-  const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
   const size_t ui = (size_t)b * (k + 1) + ipos;   // unit index within [B, k+1]
   const size_t pi = (size_t)b * k + ipos;         // position index within [B, k]
-  const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
-
-  if (g.rank == 0 && tid == 0) {
-    UnitStat st;
-    st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
-    st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
-    P.ws_stat[ui] = st;
-    if (status != 0 || greedy) {
-      if (!P.tv_only && status == 0) {
-        P.ws_y[ui] = A_t;
-        if (PAIR) {
-          P.ws_acc[pi] = x == A_t;
-          if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
-          if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
+  Merged& mg = S.mg[set1];
+  if (warp == 0) {
+    // Cluster merge (warp 0 only): lane l holds items l and l + 32.
+    mbar_wait_cluster_bounded(xbar, xpar, P.flags);
+    X1 ia, ib;
+    {
+      X1 z;
+      z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
+      z.ref_t = NO_REF; z.ref_d = NO_REF;
+      ia = lane < g.items ? S.x1[set1][lane] : z;
+      ib = lane + 32 < g.items ? S.x1[set1][lane + 32] : z;
+    }
+    const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+    const float M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
+    int A_t = 0, A_d = 0, IR_t = NO_REF, IR_d = NO_REF;
+    float S_t = 0.0f, S_d = 0.0f;
+    if (greedy) {
+      A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
+      if (PAIR)
+        A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
+    } else {
+      // the row reference is the largest item reference (ceil is monotonic)
+      IR_t = warp_max_s32(max(ia.ref_t, ib.ref_t));
+      if (PAIR) {
+        IR_d = warp_max_s32(max(ia.ref_d, ib.ref_d));
+        const u64 st = add2(pk(ia.s_t * pow2_diff(ia.ref_t, IR_t), ia.s_d * pow2_diff(ia.ref_d, IR_d)),
+                            pk(ib.s_t * pow2_diff(ib.ref_t, IR_t), ib.s_d * pow2_diff(ib.ref_d, IR_d)));
+        upk(st, S_t, S_d);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float a = __shfl_xor_sync(FULL, S_t, o), bb = __shfl_xor_sync(FULL, S_d, o);
+          upk(add2(pk(S_t, S_d), pk(a, bb)), S_t, S_d);
+        }
+      } else {
+        S_t = warp_sum_f32(ia.s_t * pow2_diff(ia.ref_t, IR_t) + ib.s_t * pow2_diff(ib.ref_t, IR_t));
+      }
+    }
+    const float R_t = IR_t == NO_REF ? 0.0f : (float)IR_t, R_d = IR_d == NO_REF ? 0.0f : (float)IR_d;
+    bool row_ok = isfinite(M_t) && (!PAIR || isfinite(M_d));
+    if (!greedy) {
+      row_ok = row_ok && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
+      if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
+    }
+    const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
+    const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
+    if (lane == 0) {
+      Merged m;
+      m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.pad = 0;
+      mg = m;
+      if (g.rank == 0) {
+        UnitStat st;
+        st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
+        st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
+        P.ws_stat[ui] = st;
+        if (status != 0 || greedy) {
+          if (!P.tv_only && status == 0) {
+            P.ws_y[ui] = A_t;
+            if (PAIR) {
+              P.ws_acc[pi] = x == A_t;
+              if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
+              if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
+            }
+          }
+          if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
         }
       }
-      if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
     }
+    __syncwarp();
+    merged_arrive();
+  } else {
+    merged_wait();
   }
-  if (status != 0 || greedy) return;   // cluster-uniform
-  if (lane == 0)   // this range's part of S_t (for a draw from p when the residual is zero)
-    P.ws_p[ui * ITEMS_MAX + g.rank * NWARP + warp] = mine.s_t * pow2_int(ref_of(mine.m_t, c) - R_t);
+  const Merged M = mg;
+  if (M.status != 0 || greedy) return;   // cluster-uniform
 
-  // ---------------- pass B: residual (pair) or target (bonus) mass of this warp's range
+  // this range's part of S_t (the target mass, and the draw from p when the residual is zero)
+  const float pmass = mine.s_t * pow2_diff(mine.ref_t, M.IR_t);
+  const size_t item = ui * ITEMS_MAX + g.rank * NWARP + warp;
+  if (!PAIR) {   // the bonus row: its mass is already known
+    if (lane == 0) { P.ws_p[item] = pmass; P.ws_w[item] = pmass; }
+    return;
+  }
+  if (lane == 0) P.ws_p[item] = pmass;
+
+  // ---------------- pass B: residual mass of this warp's range
   const u64 cc = pk(c, c);
-  const u64 nrt = pk(-R_t, -R_t), nrd = pk(-R_d, -R_d);
-  const u64 nr = pk(-r_f, -r_f);
+  const u64 nrt = pk(-M.R_t, -M.R_t), nrd = pk(-M.R_d, -M.R_d);
+  const u64 nr = pk(-M.r, -M.r);
   float w0 = 0.0f, w1 = 0.0f;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
-    const float wj = vec_weight_sum<Tl, PAIR>(rt[j], rd[PAIR ? j : 0], cc, nrt, nrd, nr);
+    const float wj = vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr);
     if (j & 1) w1 += wj; else w0 += wj;
   }
   const float wwarp = warp_sum_f32(w0 + w1);
-  if (lane == 0) P.ws_w[ui * ITEMS_MAX + g.rank * NWARP + warp] = wwarp;
-  if (PAIR && own_x && tid == 0) {   // accept test at the drafted token
-    const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
-    const float ratio = exp2f(lpx - lqx) * (S_d / S_t);
+  if (lane == 0) P.ws_w[item] = wwarp;
+  if (own_x && tid == 0) {   // accept test at the drafted token
+    const float lpx = fmaf(S.gz_t, c, -M.R_t), lqx = fmaf(S.gz_d, c, -M.R_d);
+    const float ratio = exp2f(lpx - lqx) * (M.S_d / M.S_t);
     const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
     P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
-    if (P.out_p) P.out_p[pi] = exp2f(lpx) / S_t;
-    if (P.out_q) P.out_q[pi] = exp2f(lqx) / S_d;
+    if (P.out_p) P.out_p[pi] = exp2f(lpx) / M.S_t;
+    if (P.out_q) P.out_q[pi] = exp2f(lqx) / M.S_d;
   }
 }
 
@@ -631,8 +657,9 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   g.vbeg = warp * P.wv;
   g.vend = min(g.vbeg + P.wv, g.nvec);
   const unsigned cid = cl_id(), ncl = cl_count();
-  const int upc = P.units_per_chain, k = P.k;
-  const long long n_units = (long long)P.B * upc;
+  const int k = P.k;
+  const unsigned B = (unsigned)P.B;
+  const unsigned n_units = B * (unsigned)P.units_per_chain;   // below 2^31 (checked on the host)
   const uint32_t bar = saddr(&S.bar);
   const uint4* blk_t = reinterpret_cast<const uint4*>(stage) + (size_t)(0 * NWARP + warp) * R * 32;
   const uint4* blk_d = reinterpret_cast<const uint4*>(stage) + (size_t)(1 * NWARP + warp) * R * 32;
@@ -652,18 +679,34 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   __syncthreads();
   cluster_sync_all();   // every peer's shared memory is live before the first remote store
 
-  long long u = cid;
-  if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, u, bar, stage);
+  unsigned u = cid;
+  Unit cur = unit_of(u, B);
+  if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
+  // Per-unit scalars (temperature, drafted token) are loaded one unit ahead,
+  // so their latency is hidden behind a whole unit of work.
+  float T_next = 0.0f;
+  int x_next = 0;
+  if (u < n_units) {
+    T_next = P.temperature[cur.b];
+    x_next = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
+  }
   for (; u < n_units; u += ncl, phase ^= 1u) {
-    const int b = (int)(u / upc), ipos = (int)(u % upc);
-    const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
-    const bool tma_next = P.tma && u + ncl < n_units;
-    if (ipos < k)
-      process_unit<Tl, R, true>(P, S, blk_t, blk_d, g, u, b, ipos, trow, drow, phase, n1, bar, stage, u + ncl, tma_next);
+    const bool has_next = u + ncl < n_units;
+    const Unit next = unit_of(u + ncl, B);
+    const float T = T_next;
+    const int x = x_next;
+    if (has_next) {
+      T_next = P.temperature[next.b];
+      x_next = next.ipos < k && !P.tv_only ? P.tokens[(size_t)next.b * k + next.ipos] : 0;
+    }
+    const bool tma_next = P.tma && has_next;
+    if (cur.ipos < k)
+      process_unit<Tl, R, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
     else
-      process_unit<Tl, R, false>(P, S, blk_t, blk_d, g, u, b, ipos, trow, drow, phase, n1, bar, stage, u + ncl, tma_next);
+      process_unit<Tl, R, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+    cur = next;
   }
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
 }
@@ -1091,6 +1134,7 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   if (max_batch < 0) return SV_ERR_ARG;
   if (logit_dtype != SV_FP32 && logit_dtype != SV_BF16) return SV_ERR_DTYPE;
   if (k < 1 || k > 31 || vocab < 1) return SV_ERR_SIZE;
+  if ((long long)max_batch * (k + 1) >= (1LL << 31)) return SV_ERR_SIZE;   // units are counted in 32 bits
   const int es = logit_dtype == SV_FP32 ? 4 : 2;
   const int epv = 16 / es;
   // cluster size: the largest of 8/4/2/1 that still gives each CTA a full round
