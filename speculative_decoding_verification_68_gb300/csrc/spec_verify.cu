@@ -375,10 +375,13 @@ __device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr
 // own block of R*32 vectors; the tail past the range stays -inf, so the
 // copy into registers needs no bounds checks.
 struct Geo {
-  unsigned C, rank;
-  int items;
-  long long slice0;
-  int slen, nvec, vbeg, vend;
+  const KParams* p;
+  __device__ __forceinline__ unsigned C() const { return cl_size(); }
+  __device__ __forceinline__ unsigned rank() const { return cl_rank(); }
+  __device__ __forceinline__ int items() const { return (int)cl_size() * NWARP; }
+  __device__ __forceinline__ int slice0() const { return (int)cl_rank() * p->Vs; }
+  __device__ __forceinline__ int slen() const { return max(0, min(p->Vs, p->V - slice0())); }
+  __device__ __forceinline__ int vbeg() const { return (int)(threadIdx.x >> 5) * p->wv; }
 };
 
 // Units are taken position-major, u = ipos * B + b, so that every cluster's
@@ -395,6 +398,8 @@ __device__ __forceinline__ Unit unit_of(unsigned u, unsigned B) {
   return r;
 }
 
+template <typename Tl> __device__ __forceinline__ int nvec_of(const Geo& g) { return (g.slen() + Lay<Tl>::EPV - 1) / Lay<Tl>::EPV; }
+
 // Bulk copies of one unit into the warp blocks of the stage, issued by one
 // whole warp: lane 0 arms the mbarrier with the byte count, then lane w
 // copies warp w's range of the target row and lane 8 + w that of the draft row.
@@ -408,7 +413,7 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic accesses of the stage first
   const long long trow = (long long)n.b * (k + 1) + n.ipos, drow = (long long)n.b * k + n.ipos;
   if (lane == 0) {
-    const unsigned bytes = (unsigned)g.nvec * 16u;
+    const unsigned bytes = (unsigned)nvec_of<Tl>(g) * 16u;
     if (bytes > 0) mbar_expect_tx(bar, pair ? 2 * bytes : bytes);
     else mbar_arrive(bar);
   }
@@ -416,10 +421,10 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
   const int w = lane & 7, row = lane >> 3;
   if (lane < 16 && (row == 0 || pair)) {
     const int vb = w * P.wv;
-    const int len = max(0, min(P.wv, g.nvec - vb));
+    const int len = max(0, min(P.wv, nvec_of<Tl>(g) - vb));
     if (len > 0) {
       const char* src = (const char*)(row == 0 ? P.target : P.draft) +
-                        ((size_t)(row == 0 ? trow : drow) * P.V + g.slice0) * ES + (size_t)vb * 16;
+                        ((size_t)(row == 0 ? trow : drow) * P.V + g.slice0()) * ES + (size_t)vb * 16;
       const uint32_t dst = saddr(stage + ((size_t)(row * NWARP + w) * R * 32) * 16);
       bulk_g2s(dst, src, (unsigned)len * 16u, bar);
     }
@@ -451,9 +456,9 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       rt[j] = blk_t[j * 32 + lane];
       if (PAIR) rd[j] = blk_d[j * 32 + lane];
     }
-    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0 && (long long)x < g.slice0 + g.slen;
+    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
-      const int lx = (int)(x - g.slice0);
+      const int lx = (int)(x - g.slice0());
       const int lv = lx / EPV, wb = lv / P.wv, iv = lv - wb * P.wv;
       const unsigned char* bt = smem_stage + ((size_t)(0 * NWARP + wb) * R * 32 + iv) * 16;
       const unsigned char* bd = smem_stage + ((size_t)(1 * NWARP + wb) * R * 32 + iv) * 16;
@@ -467,15 +472,15 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     if (last && tma_next) issue_unit_load<Tl, R>(P, g, next, bar, smem_stage);
   } else {
     const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
-    const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0) * ES;
-    const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0) * ES;
+    const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0()) * ES;
+    const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0()) * ES;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const int v = g.vbeg + j * 32 + lane;
-      rt[j] = load_vec_direct<Tl>(tb, v, g.slen, v < g.vend);
-      if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen, v < g.vend);
+      const int v = g.vbeg() + j * 32 + lane;
+      rt[j] = load_vec_direct<Tl>(tb, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
+      if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
     }
-    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0 && (long long)x < g.slice0 + g.slen;
+    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
       S.gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
       S.gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
@@ -506,7 +511,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     for (int j = R - 1; j >= 0; --j) {
 #pragma unroll
       for (int e = EPV - 1; e >= 0; --e) {
-        const int gi = (int)g.slice0 + (g.vbeg + j * 32 + lane) * EPV + e;
+        const int gi = (int)g.slice0() + (g.vbeg() + j * 32 + lane) * EPV + e;
         if (Lay<Tl>::elem(rt[j], e) == mine.m_t) ci_t = gi;
         if (PAIR && Lay<Tl>::elem(rd[j], e) == mine.m_d) ci_d = gi;
       }
@@ -526,9 +531,9 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   }
   const int set1 = n1 & 1;
   const uint32_t xbar = saddr(&S.xbar[set1]);
-  if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items * 32u);
-  if (lane < (int)g.C)
-    st_async_x1(peer_addr(saddr(&S.x1[set1][g.rank * NWARP + warp]), lane), mine, peer_addr(xbar, lane));
+  if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items() * 32u);
+  if (lane < (int)g.C())
+    st_async_x1(peer_addr(saddr(&S.x1[set1][g.rank() * NWARP + warp]), lane), mine, peer_addr(xbar, lane));
   const unsigned xpar = (unsigned)((n1 >> 1) & 1);
   ++n1;
 
@@ -543,8 +548,8 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       X1 z;
       z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0x7fffffff; z.i_d = 0x7fffffff;
       z.ref_t = NO_REF; z.ref_d = NO_REF;
-      ia = lane < g.items ? S.x1[set1][lane] : z;
-      ib = lane + 32 < g.items ? S.x1[set1][lane + 32] : z;
+      ia = lane < g.items() ? S.x1[set1][lane] : z;
+      ib = lane + 32 < g.items() ? S.x1[set1][lane + 32] : z;
     }
     const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
     const float M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
@@ -583,7 +588,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       Merged m;
       m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.pad = 0;
       mg = m;
-      if (g.rank == 0) {
+      if (g.rank() == 0) {
         UnitStat st;
         st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
         st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
@@ -611,7 +616,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
 
   // this range's part of S_t (the target mass, and the draw from p when the residual is zero)
   const float pmass = mine.s_t * pow2_diff(mine.ref_t, M.IR_t);
-  const size_t item = ui * ITEMS_MAX + g.rank * NWARP + warp;
+  const size_t item = ui * ITEMS_MAX + g.rank() * NWARP + warp;
   if (!PAIR) {   // the bonus row: its mass is already known
     if (lane == 0) { P.ws_p[item] = pmass; P.ws_w[item] = pmass; }
     return;
@@ -648,14 +653,7 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
 
   const int tid = threadIdx.x, warp = tid >> 5;
   Geo g;
-  g.C = cl_size();
-  g.rank = cl_rank();
-  g.items = (int)g.C * NWARP;
-  g.slice0 = (long long)g.rank * P.Vs;
-  g.slen = (int)max(0LL, min((long long)P.Vs, (long long)P.V - g.slice0));
-  g.nvec = (g.slen + Lay<Tl>::EPV - 1) / Lay<Tl>::EPV;
-  g.vbeg = warp * P.wv;
-  g.vend = min(g.vbeg + P.wv, g.nvec);
+  g.p = &P;
   const unsigned cid = cl_id(), ncl = cl_count();
   const int k = P.k;
   const unsigned B = (unsigned)P.B;
@@ -686,21 +684,11 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   int n1 = 0;   // exchanges performed (selects the slot set)
   // Per-unit scalars (temperature, drafted token) are loaded one unit ahead,
   // so their latency is hidden behind a whole unit of work.
-  float T_next = 0.0f;
-  int x_next = 0;
-  if (u < n_units) {
-    T_next = P.temperature[cur.b];
-    x_next = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
-  }
   for (; u < n_units; u += ncl, phase ^= 1u) {
     const bool has_next = u + ncl < n_units;
     const Unit next = unit_of(u + ncl, B);
-    const float T = T_next;
-    const int x = x_next;
-    if (has_next) {
-      T_next = P.temperature[next.b];
-      x_next = next.ipos < k && !P.tv_only ? P.tokens[(size_t)next.b * k + next.ipos] : 0;
-    }
+    const float T = P.temperature[cur.b];
+    const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
     const bool tma_next = P.tma && has_next;
     if (cur.ipos < k)
       process_unit<Tl, R, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
