@@ -59,6 +59,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.so_accept.argtypes = [d, d, d, ctypes.POINTER(ctypes.c_int)]
     lib.so_sample.restype = i64
     lib.so_sample.argtypes = [vp, i64, d, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+    lib.so_entropy.restype = d
+    lib.so_entropy.argtypes = [vp, ctypes.c_int, i64, d]
+    lib.so_entropy_batch.restype = ctypes.c_int
+    lib.so_entropy_batch.argtypes = [i64, i32, i64, i32, vp, vp, vp, vp, vp, ctypes.c_int]
     lib.so_verify_batch.restype = ctypes.c_int
     lib.so_verify_batch.argtypes = [i64, i32, i64, i32, vp, vp, vp, vp, vp, i32,
                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
@@ -109,6 +113,27 @@ class Oracle:
             return p
         lp, _ = self.log_softmax(z, T, dtype)
         return np.exp(lp)
+
+    def entropy(self, z, T: float, dtype: int = FP32) -> float:
+        """Entropy (nats) of one row's distribution at temperature T (0 at T == 0)."""
+        a = self._row(z, dtype)
+        return float(self.lib.so_entropy(a.ctypes.data, dtype, a.shape[-1], float(T)))
+
+    def entropy_batch(self, target, draft, temperature, dtype: int, nthreads: int = 1):
+        """Entropies of every target row [B,k+1] and draft row [B,k] (fp64)."""
+        tgt = self._row(target, dtype)
+        dft = self._row(draft, dtype)
+        B, k1, V = tgt.shape
+        k = k1 - 1
+        assert dft.shape == (B, k, V)
+        T = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+        ent_t = np.empty((B, k + 1))
+        ent_d = np.empty((B, k))
+        rc = self.lib.so_entropy_batch(B, k, V, dtype, tgt.ctypes.data, dft.ctypes.data, T.ctypes.data,
+                                       ent_t.ctypes.data, ent_d.ctypes.data, int(nthreads))
+        if rc != 0:
+            raise ValueError(f"so_entropy_batch failed: {rc}")
+        return ent_t, ent_d
 
     def accept(self, lp: float, lq: float, u: float):
         tie = ctypes.c_int(0)

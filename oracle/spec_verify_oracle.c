@@ -290,6 +290,74 @@ int so_verify_chain(const so_chain_in* in, so_chain_out* out) {
   return 0;
 }
 
+/* Entropy, in nats, of one row's distribution at temperature T:
+ *   H = -sum_j p_j log p_j,  p = softmax(z / T).
+ * The pages tie acceptance degradation to fluctuations in the model's output
+ * entropy, "how spread out the token probabilities are" (page 1 and page 2,
+ * section "Rejection sampling and a loss that optimizes acceptance
+ * directly"); they print no formula, and Shannon entropy of the distribution
+ * the verifier uses is the reading.  Entries with p_j = 0 (logit -inf) add
+ * nothing (0 log 0 = 0).  T == 0: the greedy one-hot distribution, H = 0.
+ * NaN for a temperature that is NaN, infinite or negative, or a row whose
+ * maximum is not finite. */
+double so_entropy(const void* row, int dtype, int64_t V, double T) {
+  if (!(T >= 0.0) || isinf(T)) return NAN;
+  if (!isfinite(row_max(row, dtype, V))) return NAN;
+  if (T == 0.0) return 0.0;
+  double lse = so_log_softmax(row, dtype, V, T, NULL);
+  double h = 0.0;
+  for (int64_t j = 0; j < V; ++j) {
+    double lp = logit_at(row, dtype, j) / T - lse;
+    if (lp > -INFINITY) h -= exp(lp) * lp;
+  }
+  return h;
+}
+
+/* Entropies of every target row [B, k+1] and draft row [B, k] of a batch,
+ * each row with its chain's temperature (rows split over threads). */
+typedef struct {
+  int64_t B, V;
+  int32_t k, dtype;
+  const void* target; const void* draft; const float* T;
+  double* ent_t; double* ent_d;
+  int64_t first, stride;
+} so_entropy_job;
+
+static void* entropy_worker(void* arg) {
+  so_entropy_job* J = (so_entropy_job*)arg;
+  const size_t rs = (size_t)J->V * (J->dtype == SO_FP32 ? 4 : 2);
+  const int64_t rows = J->B * (2 * (int64_t)J->k + 1);
+  for (int64_t r = J->first; r < rows; r += J->stride) {
+    const int64_t b = r / (2 * J->k + 1), i = r % (2 * J->k + 1);
+    const double T = (double)J->T[b];
+    if (i <= J->k)
+      J->ent_t[b * (J->k + 1) + i] = so_entropy((const char*)J->target + (size_t)(b * (J->k + 1) + i) * rs, J->dtype, J->V, T);
+    else
+      J->ent_d[b * J->k + (i - J->k - 1)] =
+          so_entropy((const char*)J->draft + (size_t)(b * J->k + (i - J->k - 1)) * rs, J->dtype, J->V, T);
+  }
+  return NULL;
+}
+
+int so_entropy_batch(int64_t B, int32_t k, int64_t V, int32_t dtype, const void* target, const void* draft,
+                     const float* T, double* ent_t, double* ent_d, int nthreads) {
+  if (B < 0 || k < 1 || V < 1 || (dtype != SO_FP32 && dtype != SO_BF16)) return 1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  so_entropy_job jobs[256];
+  pthread_t th[256];
+  for (int t = 0; t < nthreads; ++t) jobs[t] = (so_entropy_job){B, V, k, dtype, target, draft, T, ent_t, ent_d, t, nthreads};
+  if (nthreads == 1) { entropy_worker(&jobs[0]); return 0; }
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, entropy_worker, &jobs[t]) != 0) break;
+    started++;
+  }
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  for (int t = started; t < nthreads; ++t) entropy_worker(&jobs[t]);
+  return 0;
+}
+
 /* ---- batch driver (chains statically partitioned over threads) ------ */
 typedef struct {
   int64_t B, V;

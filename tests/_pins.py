@@ -16,6 +16,7 @@ mistake) and raises AssertionError when the oracle disagrees with:
 from __future__ import annotations
 
 import json
+import math
 import os
 
 import numpy as np
@@ -292,5 +293,48 @@ def pin_inverse_cdf_library(orc):
     assert orc.sample(w, 0.0)[0] == 1         # the first positive weight, not index 0
 
 
+def pin_entropy_closed_forms(orc):
+    """Entropy of rows whose distribution is known in closed form: a constant
+    row is uniform (H = ln V); a row with n_a logits a and n_b logits b has two
+    probability levels; -inf logits are masked out; T == 0 gives 0."""
+    for V in (1, 2, 16, 1000, 151552):
+        for T in (0.3, 1.0, 2.5):
+            h = orc.entropy(np.full(V, 1.25, np.float32), T)
+            # fp64 sum of V equal terms: rounding grows like V * eps
+            assert abs(h - math.log(V)) <= 1e-15 * V * max(1.0, math.log(V)), (V, T, h)
+    for n_a, n_b, a, b, T in ((1, 15, 3.0, 0.0, 1.0), (5, 995, 2.0, -1.0, 0.7), (100, 100, 0.0, -4.0, 2.0),
+                              (1, 4095, 9.0, 0.0, 0.6)):
+        z = np.concatenate([np.full(n_a, a), np.full(n_b, b)]).astype(np.float32)
+        ea, eb = math.exp(a / T), math.exp(b / T)
+        pa, pb = ea / (n_a * ea + n_b * eb), eb / (n_a * ea + n_b * eb)
+        want = -(n_a * pa * math.log(pa) + n_b * pb * math.log(pb))
+        assert abs(orc.entropy(z, T) - want) <= 1e-12, (n_a, n_b, a, b, T)
+        masked = np.concatenate([z, np.full(37, -np.inf, np.float32)])
+        assert abs(orc.entropy(masked, T) - want) <= 1e-12
+    assert orc.entropy(np.array([0.0, 3.0, 3.0], np.float32), 0.0) == 0.0
+    assert math.isnan(orc.entropy(np.array([0.0, np.nan], np.float32), 1.0))
+    assert math.isnan(orc.entropy(np.array([0.0, 1.0], np.float32), -1.0))
+
+
+def pin_entropy_library(orc):
+    """H = scipy.stats.entropy of scipy's softmax(z / T), on random rows (fp32 and
+    bf16 storage); 0 <= H <= ln V, and H grows with T."""
+    import scipy.special
+    import scipy.stats
+    rng = np.random.default_rng(17)
+    for V, T, s in ((16, 1.0, 2.0), (1000, 0.6, 3.0), (4096, 1.7, 0.5), (30000, 1.0, 4.0)):
+        z = (rng.standard_normal(V) * s).astype(np.float32)
+        want = scipy.stats.entropy(scipy.special.softmax(z.astype(np.float64) / T))
+        got = orc.entropy(z, T)
+        assert abs(got - want) <= 1e-11 * max(1.0, want), (V, T, got, want)
+        assert 0.0 <= got <= math.log(V) + 1e-12
+        assert orc.entropy(z, 0.5 * T) < got < orc.entropy(z, 2.0 * T)
+        zb = z.view(np.uint32) >> 16 << 16        # a bf16 row: the oracle reads the high half
+        bf = (zb >> 16).astype(np.uint16)
+        want_b = scipy.stats.entropy(scipy.special.softmax(zb.view(np.float32).astype(np.float64) / T))
+        assert abs(orc.entropy(bf, T, dtype=1) - want_b) <= 1e-11 * max(1.0, want_b)
+
+
 ALL_PINS = [pin_worked_examples, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
-            pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact]
+            pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact,
+            pin_entropy_closed_forms, pin_entropy_library]

@@ -25,6 +25,10 @@ MUTANTS = {
     "argmax_last_of_ties": ("if (z > m) { m = z; a = j; }", "if (z >= m) { m = z; a = j; }"),
     "cdf_not_strict": ("if (t < C) { y = j; break; }", "if (t <= C) { y = j; break; }"),
     "lse_missing_max": ("double lse = lmax + log(s);", "double lse = log(s);"),
+    "entropy_in_bits": ("if (lp > -INFINITY) h -= exp(lp) * lp;", "if (lp > -INFINITY) h -= exp(lp) * lp / log(2.0);"),
+    "entropy_sign_flipped": ("if (lp > -INFINITY) h -= exp(lp) * lp;", "if (lp > -INFINITY) h += exp(lp) * lp;"),
+    "entropy_without_temperature": ("double lp = logit_at(row, dtype, j) / T - lse;",
+                                    "double lp = logit_at(row, dtype, j) - lse;"),
 }
 
 
