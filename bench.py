@@ -370,6 +370,22 @@ def main(argv=None):
                                "mean_tau": float(oo["tau"].float().mean().item())}
             so.close()
             del di, oo
+        # the main workload again through spec_verify_ex: verification plus the entropy of every row
+        wo = w0 if w0.batch <= 1024 else w0.scaled(batch=1024)
+        bo = si.generate(wo)
+        di = device_batch(bo, device)
+        so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16" if wo.dtype == si.BF16 else "fp32",
+                                flags=svlib.SV_FLAG_KERNEL_TIMING)
+        oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device, want_entropy=True)
+        for _ in range(3):
+            so.verify(*di, out=oo)
+        kms, _ = measure_kernel(so, di, oo, 20, flush=flush)
+        ob = wo.logit_bytes
+        others[wo.name + "+entropy"] = {"kernel_us": 1e3 * kms, "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
+                                        "gbps": ob / (kms / 1e3) / 1e9, "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
+                                        "api": "spec_verify_ex (entropy of every target and draft row)"}
+        so.close()
+        del di, oo, bo
         del flush
 
     cpu = None

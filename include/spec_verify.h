@@ -109,6 +109,29 @@ int spec_verify(spec_verify_t h, int batch,
                 float* out_p_draft, float* out_q_draft, float* out_tv,
                 void* cuda_stream);
 
+/* spec_verify, and also the entropy of every logit row's distribution, in
+ * the same pass over the logits.  The pages tie the fall of acceptance to
+ * fluctuations in the model's output entropy, "how spread out the token
+ * probabilities are" ("Optimizing speculative decoding" and "GLM-5.2: Tuning
+ * MTP speculative decoding to the limit", section "Rejection sampling and a
+ * loss that optimizes acceptance directly"); the statistic here is the
+ * Shannon entropy, in nats, of p = softmax(z / T), the distribution the
+ * verifier itself uses:
+ *   out_entropy_target [batch, k+1] fp32: H of target row i
+ *   out_entropy_draft  [batch, k]   fp32: H of draft row i
+ * Both NULL (then this is spec_verify) or both non-NULL and 4-byte aligned,
+ * else SV_ERR_ARG.  H = 0 for greedy chains (T == 0).  H = NaN for a chain
+ * with an invalid temperature, and for a row without a finite maximum.
+ * Masked logits (-inf) add nothing.  The other outputs are bit-identical to
+ * spec_verify's.  Two kernel launches. */
+int spec_verify_ex(spec_verify_t h, int batch,
+                   const void* target_logits, const void* draft_logits,
+                   const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_tau,
+                   float* out_p_draft, float* out_q_draft, float* out_tv,
+                   float* out_entropy_target, float* out_entropy_draft,
+                   void* cuda_stream);
+
 /* Allocation-free spec_verify.  The pages have no counterpart of this call;
  * it exists for callers that cannot allocate device memory.  cudaMalloc may
  * synchronise the whole device, and a serving engine that has reserved its

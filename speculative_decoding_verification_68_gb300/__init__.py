@@ -89,7 +89,8 @@ class SpecVerifier:
             stream = torch.cuda.current_stream()
         return ctypes.c_void_p(stream.cuda_stream)
 
-    def alloc_outputs(self, batch: int, want_pq: bool = True, want_tv: bool = False, device="cuda") -> dict:
+    def alloc_outputs(self, batch: int, want_pq: bool = True, want_tv: bool = False, device="cuda",
+                      want_entropy: bool = False) -> dict:
         import torch
         k = self.k
         out = {"tokens": torch.empty((batch, k + 1), dtype=torch.int32, device=device),
@@ -99,6 +100,9 @@ class SpecVerifier:
             out["q_draft"] = torch.empty((batch, k), dtype=torch.float32, device=device)
         if want_tv:
             out["tv"] = torch.empty((batch, k), dtype=torch.float32, device=device)
+        if want_entropy:
+            out["entropy_target"] = torch.empty((batch, k + 1), dtype=torch.float32, device=device)
+            out["entropy_draft"] = torch.empty((batch, k), dtype=torch.float32, device=device)
         return out
 
     def _check_inputs(self, target, draft, tokens, temperature, uniforms):
@@ -116,15 +120,23 @@ class SpecVerifier:
         return B
 
     def verify(self, target, draft, tokens, temperature, uniforms, want_pq: bool = True, want_tv: bool = False,
-               out: dict | None = None, stream=None) -> dict:
-        """Verify a batch of chains held in CUDA tensors; returns output tensors (asynchronous)."""
+               out: dict | None = None, stream=None, want_entropy: bool = False) -> dict:
+        """Verify a batch of chains held in CUDA tensors; returns output tensors (asynchronous).
+        With want_entropy (or entropy tensors in `out`) this is spec_verify_ex, which also
+        writes the entropy of every target and draft row."""
         B = self._check_inputs(target, draft, tokens, temperature, uniforms)
         if out is None:
-            out = self.alloc_outputs(B, want_pq, want_tv, device=target.device)
-        rc = self._lib.spec_verify(self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature),
-                                   _ptr(uniforms), _ptr(out["tokens"]), _ptr(out["tau"]), _ptr(out.get("p_draft")),
-                                   _ptr(out.get("q_draft")), _ptr(out.get("tv")), self._stream(stream))
-        _check(rc, "spec_verify")
+            out = self.alloc_outputs(B, want_pq, want_tv, device=target.device, want_entropy=want_entropy)
+        args = (self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature), _ptr(uniforms),
+                _ptr(out["tokens"]), _ptr(out["tau"]), _ptr(out.get("p_draft")), _ptr(out.get("q_draft")),
+                _ptr(out.get("tv")))
+        if "entropy_target" in out or "entropy_draft" in out:
+            rc = self._lib.spec_verify_ex(*args, _ptr(out.get("entropy_target")), _ptr(out.get("entropy_draft")),
+                                          self._stream(stream))
+            _check(rc, "spec_verify_ex")
+        else:
+            rc = self._lib.spec_verify(*args, self._stream(stream))
+            _check(rc, "spec_verify")
         return out
 
     def verify_tv(self, target, draft, temperature, out=None, stream=None):

@@ -49,6 +49,7 @@ constexpr int CMAX = 8;            // largest cluster
 constexpr int ITEMS_MAX = CMAX * NWARP;
 constexpr int SMALL_BYTES = 4352;  // bookkeeping area in front of the stage
 constexpr float LOG2E_F = 1.44269504088896341f;
+constexpr float LN2_F = 0.69314718055994531f;
 constexpr float REF_LIMIT = 4194304.0f;   // |max * c| must stay below 2^22
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -76,6 +77,8 @@ struct KParams {
   float* out_p;              // [B, k] or null
   float* out_q;              // [B, k] or null
   float* out_tv;             // [B, k] or null (greedy units only; others in finalize)
+  float* out_ent_t;          // [B, k+1] per-row entropy of the target rows (entropy kernels only)
+  float* out_ent_d;          // [B, k]   per-row entropy of the draft rows (entropy kernels only)
   int32_t* ws_acc;           // [B, k]
   int32_t* ws_y;             // [B, k+1] greedy tokens
   UnitStat* ws_stat;         // [B, k+1]
@@ -367,6 +370,58 @@ __device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr
   return l0 + h0;
 }
 
+// As rows_expsum, and also sum e*a over the same elements, e = 2^a with
+// a = z*c + nref (the log2-domain logit relative to the reference): the
+// second moment the row entropy needs, H = ln S - ln2 * (sum e*a) / S.
+// a is clamped at -127 so that a masked logit (-inf) adds 0 * -127 instead
+// of 0 * -inf; every e is unchanged, since ex2 flushes 2^a to 0 below -126.
+__device__ __forceinline__ u64 clamp_m127(u64 x) {
+  float lo, hi;
+  upk(x, lo, hi);
+  return pk(fmaxf(lo, -127.0f), fmaxf(hi, -127.0f));
+}
+template <typename Tl, int R>
+__device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, float& ea) {
+  u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
+  u64 m0 = 0ull, m1 = 0ull, m2 = 0ull, m3 = 0ull;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    u64 x0, x1, x2, x3;
+    if constexpr (sizeof(Tl) == 4) {
+      x0 = clamp_m127(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr));
+      x1 = clamp_m127(fma2(pk(__uint_as_float(v[j].z), __uint_as_float(v[j].w)), cc, nr));
+      float p0, p1, p2, p3;
+      upk(x0, p0, p1);
+      upk(x1, p2, p3);
+      const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3));
+      if (j & 1) { a2 = add2(a2, e0); a3 = add2(a3, e1); m2 = fma2(e0, x0, m2); m3 = fma2(e1, x1, m3); }
+      else { a0 = add2(a0, e0); a1 = add2(a1, e1); m0 = fma2(e0, x0, m0); m1 = fma2(e1, x1, m1); }
+    } else {
+      x0 = clamp_m127(fma2(pk(bf_lo(v[j].x), bf_hi(v[j].x)), cc, nr));
+      x1 = clamp_m127(fma2(pk(bf_lo(v[j].y), bf_hi(v[j].y)), cc, nr));
+      x2 = clamp_m127(fma2(pk(bf_lo(v[j].z), bf_hi(v[j].z)), cc, nr));
+      x3 = clamp_m127(fma2(pk(bf_lo(v[j].w), bf_hi(v[j].w)), cc, nr));
+      float p0, p1, p2, p3, p4, p5, p6, p7;
+      upk(x0, p0, p1);
+      upk(x1, p2, p3);
+      upk(x2, p4, p5);
+      upk(x3, p6, p7);
+      const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3)), e2 = pk(ex2(p4), ex2(p5)), e3 = pk(ex2(p6), ex2(p7));
+      a0 = add2(a0, e0); a1 = add2(a1, e1); a2 = add2(a2, e2); a3 = add2(a3, e3);
+      m0 = fma2(e0, x0, m0); m1 = fma2(e1, x1, m1); m2 = fma2(e2, x2, m2); m3 = fma2(e3, x3, m3);
+    }
+  }
+  float l0, h0, l1, h1;
+  upk(add2(add2(m0, m1), add2(m2, m3)), l1, h1);
+  ea = l1 + h1;
+  upk(add2(add2(a0, a1), add2(a2, a3)), l0, h0);
+  return l0 + h0;
+}
+
+// Entropy (nats) of a row from its sums relative to the row reference:
+// S = sum e, EA = sum e*a with e = 2^a (see rows_expsum_ent).
+__device__ __forceinline__ float row_entropy(float S, float EA) { return logf(S) - LN2_F * (EA / S); }
+
 // ------------------------------------------------------------- fused kernel
 // Vector v of a CTA's slice (16 bytes: EPV logits) belongs to warp v / WV,
 // round (v % WV) / 32, lane v % 32, where WV = ceil(nvec / NWARP): every warp
@@ -435,7 +490,7 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
 __device__ __forceinline__ void merged_arrive() { asm volatile("bar.arrive 1, %0;" ::"n"(NT) : "memory"); }
 __device__ __forceinline__ void merged_wait() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
-template <typename Tl, int R, bool PAIR>
+template <typename Tl, int R, bool PAIR, bool ENT>
 __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
@@ -522,11 +577,31 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     const u64 cc = pk(c, c);
     mine.ref_t = iref_of(mine.m_t, c);
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
-    mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
-    if (PAIR) {
-      mine.ref_d = iref_of(mine.m_d, c);
-      const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-      mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+    if constexpr (ENT) {   // the index fields carry sum e*a for sampling units
+      float ea_t = 0.0f, ea_d = 0.0f;
+      mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), ea_t);
+      if (PAIR) {
+        mine.ref_d = iref_of(mine.m_d, c);
+        const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
+        mine.s_d = rows_expsum_ent<Tl, R>(rd, cc, pk(-rwd, -rwd), ea_d);
+      }
+      float v0 = mine.s_t, v1 = mine.s_d, v2 = ea_t, v3 = ea_d;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float y0 = __shfl_xor_sync(FULL, v0, o), y1 = __shfl_xor_sync(FULL, v1, o);
+        const float y2 = __shfl_xor_sync(FULL, v2, o), y3 = __shfl_xor_sync(FULL, v3, o);
+        upk(add2(pk(v0, v1), pk(y0, y1)), v0, v1);
+        upk(add2(pk(v2, v3), pk(y2, y3)), v2, v3);
+      }
+      mine.s_t = v0; mine.s_d = v1;
+      mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
+    } else {
+      mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
+      if (PAIR) {
+        mine.ref_d = iref_of(mine.m_d, c);
+        const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
+        mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+      }
     }
   }
   const int set1 = n1 & 1;
@@ -584,6 +659,35 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     }
     const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
     const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
+    if constexpr (ENT) {
+      // Row entropies.  Each item's sum e*a is relative to its own reference;
+      // on the row reference it becomes 2^(ref_i - R) * (EA_i + (ref_i - R) * s_i).
+      float H_t = __int_as_float(0x7fc00000), H_d = H_t;
+      if (greedy) {   // the one-hot greedy distribution (NaN for an invalid temperature)
+        if (t_ok && isfinite(M_t)) H_t = 0.0f;
+        if (t_ok && PAIR && isfinite(M_d)) H_d = 0.0f;
+      } else {
+        auto part = [&](float s_i, float ea_i, int ref_i, int IR) {   // empty ranges and padding add 0
+          return ref_i == NO_REF ? 0.0f : pow2_diff(ref_i, IR) * fmaf((float)ref_i - (float)IR, s_i, ea_i);
+        };
+        float e_t = part(ia.s_t, __int_as_float(ia.i_t), ia.ref_t, IR_t) + part(ib.s_t, __int_as_float(ib.i_t), ib.ref_t, IR_t);
+        float e_d = PAIR ? part(ia.s_d, __int_as_float(ia.i_d), ia.ref_d, IR_d) + part(ib.s_d, __int_as_float(ib.i_d), ib.ref_d, IR_d)
+                         : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float y0 = __shfl_xor_sync(FULL, e_t, o), y1 = __shfl_xor_sync(FULL, e_d, o);
+          upk(add2(pk(e_t, e_d), pk(y0, y1)), e_t, e_d);
+        }
+        const bool ok_t = t_ok && isfinite(M_t) && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
+        const bool ok_d = t_ok && isfinite(M_d) && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
+        if (ok_t) H_t = row_entropy(S_t, e_t);
+        if (PAIR && ok_d) H_d = row_entropy(S_d, e_d);
+      }
+      if (lane == 0 && g.rank() == 0) {
+        P.out_ent_t[ui] = H_t;
+        if (PAIR) P.out_ent_d[pi] = H_d;
+      }
+    }
     if (lane == 0) {
       Merged m;
       m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.pad = 0;
@@ -645,7 +749,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   }
 }
 
-template <typename Tl, int R>
+template <typename Tl, int R, bool ENT>
 __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   Small& S = *reinterpret_cast<Small*>(smem);
@@ -691,9 +795,9 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
     const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
     const bool tma_next = P.tma && has_next;
     if (cur.ipos < k)
-      process_unit<Tl, R, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+      process_unit<Tl, R, true, ENT>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
     else
-      process_unit<Tl, R, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+      process_unit<Tl, R, false, ENT>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
     cur = next;
   }
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
@@ -890,14 +994,14 @@ constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10};
 constexpr int N_R = 6;
 
 template <typename Tl>
-void pick_kernels(int r, FusedFn& f, FinalFn& g) {
+void pick_kernels(int r, FusedFn& f, FusedFn& fe, FinalFn& g) {
   switch (r) {
-    case 1: f = sv_fused_kernel<Tl, 1>; g = sv_finalize_kernel<Tl, 1>; break;
-    case 2: f = sv_fused_kernel<Tl, 2>; g = sv_finalize_kernel<Tl, 2>; break;
-    case 4: f = sv_fused_kernel<Tl, 4>; g = sv_finalize_kernel<Tl, 4>; break;
-    case 6: f = sv_fused_kernel<Tl, 6>; g = sv_finalize_kernel<Tl, 6>; break;
-    case 8: f = sv_fused_kernel<Tl, 8>; g = sv_finalize_kernel<Tl, 8>; break;
-    default: f = sv_fused_kernel<Tl, 10>; g = sv_finalize_kernel<Tl, 10>; break;
+    case 1: f = sv_fused_kernel<Tl, 1, false>; fe = sv_fused_kernel<Tl, 1, true>; g = sv_finalize_kernel<Tl, 1>; break;
+    case 2: f = sv_fused_kernel<Tl, 2, false>; fe = sv_fused_kernel<Tl, 2, true>; g = sv_finalize_kernel<Tl, 2>; break;
+    case 4: f = sv_fused_kernel<Tl, 4, false>; fe = sv_fused_kernel<Tl, 4, true>; g = sv_finalize_kernel<Tl, 4>; break;
+    case 6: f = sv_fused_kernel<Tl, 6, false>; fe = sv_fused_kernel<Tl, 6, true>; g = sv_finalize_kernel<Tl, 6>; break;
+    case 8: f = sv_fused_kernel<Tl, 8, false>; fe = sv_fused_kernel<Tl, 8, true>; g = sv_finalize_kernel<Tl, 8>; break;
+    default: f = sv_fused_kernel<Tl, 10, false>; fe = sv_fused_kernel<Tl, 10, true>; g = sv_finalize_kernel<Tl, 10>; break;
   }
 }
 
@@ -911,6 +1015,8 @@ struct spec_verify_ctx {
   int C, Vs, R, wv, n_clusters, tma_ok;
   size_t smem;
   FusedFn kernel;
+  FusedFn kernel_ent;        // the same kernel that also writes row entropies
+  int n_clusters_ent;
   FinalFn finalize;
   int32_t* ws_acc;
   int32_t* ws_y;
@@ -951,7 +1057,9 @@ static void free_ctx(spec_verify_ctx* h) {
 }
 
 static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s) {
-  const int grid_clusters = (int)(units < h->n_clusters ? units : h->n_clusters);
+  const bool ent = P.out_ent_t || P.out_ent_d;
+  const int ncl = ent ? h->n_clusters_ent : h->n_clusters;
+  const int grid_clusters = (int)(units < ncl ? units : ncl);
   if (grid_clusters <= 0) return SV_OK;
   const bool timed = h->ev && h->ev_n < TIMING_RING;
   if (timed && cudaEventRecord(h->ev[2 * h->ev_n], s) != cudaSuccess) return SV_ERR_CUDA;
@@ -968,7 +1076,7 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, h->kernel, P) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, ent ? h->kernel_ent : h->kernel, P) != cudaSuccess) return SV_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(h->ev[2 * h->ev_n + 1], s) != cudaSuccess) return SV_ERR_CUDA;
     h->ev_n++;
@@ -1064,8 +1172,8 @@ int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) 
   h.C = C; h.Vs = (int)Vs; h.R = R; h.wv = (int)wv;
   h.tma_ok = ((size_t)vocab * es) % 16 == 0;
   h.smem = SMALL_BYTES + (h.tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
-  if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.finalize);
-  else pick_kernels<__nv_bfloat16>(R, h.kernel, h.finalize);
+  if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.finalize);
+  else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.finalize);
   if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem) != cudaSuccess)
     return SV_ERR_CUDA;
   cudaLaunchConfig_t cfg;
@@ -1147,9 +1255,10 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   h->C = C; h->Vs = (int)Vs; h->R = R; h->wv = (int)wv;
   h->tma_ok = ((size_t)vocab * es) % 16 == 0 && !(flags & SV_FLAG_NO_TMA);
   h->smem = SMALL_BYTES + (h->tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
-  if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->finalize);
-  else pick_kernels<__nv_bfloat16>(R, h->kernel, h->finalize);
-  if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
+  if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->finalize);
+  else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->finalize);
+  if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
+      cudaFuncSetAttribute(h->kernel_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
     free_ctx(h);
     return SV_ERR_CUDA;
   }
@@ -1166,13 +1275,15 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, h->kernel, &cfg) != cudaSuccess || n <= 0) {
+    int n = 0, ne = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, h->kernel, &cfg) != cudaSuccess || n <= 0 ||
+        cudaOccupancyMaxActiveClusters(&ne, h->kernel_ent, &cfg) != cudaSuccess || ne <= 0) {
       cudaGetLastError();
       free_ctx(h);
       return SV_ERR_CUDA;
     }
     h->n_clusters = n;
+    h->n_clusters_ent = ne;
   }
   const size_t mb = (size_t)(max_batch > 0 ? max_batch : 1);
   bool ok = cudaMalloc(&h->ws_acc, mb * k * sizeof(int32_t)) == cudaSuccess &&
@@ -1220,6 +1331,14 @@ int spec_verify(spec_verify_t h, int batch, const void* target_logits, const voi
                 const int32_t* draft_tokens, const float* temperature, const float* uniforms,
                 int32_t* out_tokens, int32_t* out_tau, float* out_p_draft, float* out_q_draft, float* out_tv,
                 void* cuda_stream) {
+  return spec_verify_ex(h, batch, target_logits, draft_logits, draft_tokens, temperature, uniforms, out_tokens, out_tau,
+                        out_p_draft, out_q_draft, out_tv, nullptr, nullptr, cuda_stream);
+}
+
+int spec_verify_ex(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                   const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_tau, float* out_p_draft, float* out_q_draft, float* out_tv,
+                   float* out_entropy_target, float* out_entropy_draft, void* cuda_stream) {
   if (!h || batch < 0 || batch > h->max_batch) return SV_ERR_ARG;
   if (batch == 0) return SV_OK;
   if (!target_logits || !draft_logits || !draft_tokens || !temperature || !uniforms || !out_tokens || !out_tau)
@@ -1227,13 +1346,15 @@ int spec_verify(spec_verify_t h, int batch, const void* target_logits, const voi
   const int es = h->dtype == SV_FP32 ? 4 : 2;
   if (((uintptr_t)target_logits % es) || ((uintptr_t)draft_logits % es)) return SV_ERR_ARG;
   if (!al4(draft_tokens) || !al4(temperature) || !al4(uniforms) || !al4(out_tokens) || !al4(out_tau) ||
-      !al4(out_p_draft) || !al4(out_q_draft) || !al4(out_tv))
+      !al4(out_p_draft) || !al4(out_q_draft) || !al4(out_tv) || !al4(out_entropy_target) || !al4(out_entropy_draft))
     return SV_ERR_ARG;
+  if ((out_entropy_target == nullptr) != (out_entropy_draft == nullptr)) return SV_ERR_ARG;
   cudaStream_t s = (cudaStream_t)cuda_stream;
   KParams P;
   memset(&P, 0, sizeof P);
   P.target = target_logits; P.draft = draft_logits; P.tokens = draft_tokens; P.temperature = temperature;
   P.uniforms = uniforms; P.out_p = out_p_draft; P.out_q = out_q_draft; P.out_tv = out_tv;
+  P.out_ent_t = out_entropy_target; P.out_ent_d = out_entropy_draft;
   P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
   P.flags = h->d_flags;
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
