@@ -29,6 +29,7 @@ _libs: dict[str, ctypes.CDLL] = {}
 
 FP32 = 0
 BF16 = 1
+FP64 = 2   # single-row functions only (finite differences in the tests)
 TIE_BAND = 1e-6
 
 
@@ -63,6 +64,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.so_entropy.argtypes = [vp, ctypes.c_int, i64, d]
     lib.so_entropy_batch.restype = ctypes.c_int
     lib.so_entropy_batch.argtypes = [i64, i32, i64, i32, vp, vp, vp, vp, vp, ctypes.c_int]
+    lib.so_overlap_grad.restype = ctypes.c_int
+    lib.so_overlap_grad.argtypes = [vp, vp, ctypes.c_int, i64, d, ctypes.c_int, d, vp, vp, vp, vp]
+    lib.so_overlap_grad_batch.restype = ctypes.c_int
+    lib.so_overlap_grad_batch.argtypes = [i64, i32, i64, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, ctypes.c_int]
     lib.so_verify_batch.restype = ctypes.c_int
     lib.so_verify_batch.argtypes = [i64, i32, i64, i32, vp, vp, vp, vp, vp, i32,
                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
@@ -91,7 +96,7 @@ class Oracle:
 
     @staticmethod
     def _row(z, dtype):
-        a = np.ascontiguousarray(z, dtype=np.float32 if dtype == FP32 else np.uint16)
+        a = np.ascontiguousarray(z, dtype={FP32: np.float32, BF16: np.uint16, FP64: np.float64}[dtype])
         return a
 
     def argmax(self, z, dtype: int = FP32) -> int:
@@ -134,6 +139,34 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"so_entropy_batch failed: {rc}")
         return ent_t, ent_d
+
+    def overlap_grad(self, zt, zd, T: float, kind: int, w: float = 1.0, dtype: int = FP32):
+        """(loss, alpha, grad [V], tie mass) of one position: kind 0 = TV loss 1 - alpha,
+        kind 1 = overlap loss -ln alpha; grad is d(w * loss)/d(draft logits)."""
+        a, b = self._row(zt, dtype), self._row(zd, dtype)
+        V = a.shape[-1]
+        loss, alpha, tie = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        g = np.empty(V)
+        self.lib.so_overlap_grad(a.ctypes.data, b.ctypes.data, dtype, V, float(T), int(kind), float(w),
+                                 ctypes.byref(loss), ctypes.byref(alpha), g.ctypes.data, ctypes.byref(tie))
+        return loss.value, alpha.value, g, tie.value
+
+    def overlap_grad_batch(self, target, draft, temperature, kind: int, weights=None, dtype: int = FP32,
+                           nthreads: int = 1) -> dict:
+        """Losses and draft-logit gradients of every position of a batch (fp64)."""
+        tgt, dft = self._row(target, dtype), self._row(draft, dtype)
+        B, k1, V = tgt.shape
+        k = k1 - 1
+        T = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+        w = None if weights is None else np.ascontiguousarray(weights, dtype=np.float32).reshape(B, k)
+        out = dict(loss=np.empty((B, k)), alpha=np.empty((B, k)), grad=np.empty((B, k, V)), tie=np.empty((B, k)))
+        rc = self.lib.so_overlap_grad_batch(B, k, V, dtype, tgt.ctypes.data, dft.ctypes.data, T.ctypes.data, int(kind),
+                                            None if w is None else w.ctypes.data, out["loss"].ctypes.data,
+                                            out["alpha"].ctypes.data, out["grad"].ctypes.data, out["tie"].ctypes.data,
+                                            int(nthreads))
+        if rc != 0:
+            raise ValueError(f"so_overlap_grad_batch failed: {rc}")
+        return out
 
     def accept(self, lp: float, lq: float, u: float):
         tie = ctypes.c_int(0)

@@ -54,10 +54,14 @@
 
 #define SO_FP32 0
 #define SO_BF16 1
+#define SO_FP64 2
 #define SO_TIE_BAND 1e-6
 
-/* Exact conversion of one stored logit to double (bf16 widens exactly). */
+/* Exact conversion of one stored logit to double (bf16 widens exactly).
+ * SO_FP64 rows exist for the tests' finite differences only; the batch
+ * drivers accept fp32 and bf16. */
 static double logit_at(const void* row, int dtype, int64_t j) {
+  if (dtype == SO_FP64) return ((const double*)row)[j];
   if (dtype == SO_FP32) return (double)((const float*)row)[j];
   uint32_t bits = (uint32_t)((const uint16_t*)row)[j] << 16;
   float f;
@@ -355,6 +359,104 @@ int so_entropy_batch(int64_t B, int32_t k, int64_t V, int32_t dtype, const void*
   }
   for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
   for (int t = started; t < nthreads; ++t) entropy_worker(&jobs[t]);
+  return 0;
+}
+
+/* Losses on the draft-target overlap, and their gradient with respect to the
+ * draft logits (the target is frozen).  For one position with target row zt,
+ * draft row zd and temperature T > 0, p = softmax(zt / T), q = softmax(zd / T):
+ *   alpha = sum_x min(p(x), q(x)), the probability that the protocol accepts
+ *           the drafted token (page 1, section "Kimi K3"), = 1 - TV;
+ *   kind 0, TV loss:       l = TV = 1 - alpha  (page 1 and page 2, section
+ *           "Rejection sampling and a loss that optimizes acceptance
+ *           directly", second bullet; per position is the reading);
+ *   kind 1, overlap loss:  l = -ln alpha  (page 1, section "Kimi K3": the
+ *           negative log of the draft-target overlap).
+ * With weight w the position contributes w * l to the loss, and
+ *   d(w l)/d zd_m = w * dl/dalpha * (q_m / T) * ([q_m < p_m] - beta),
+ *   beta = sum_x [q_x < p_x] q_x,
+ * since d min(p_x, q_x)/d q_x = [q_x < p_x] (the strict side at a tie) and
+ * d q_x / d zd_m = q_x (delta_xm - q_m) / T.  dl/dalpha is -1 (TV) or
+ * -1/alpha (overlap).  `tie` returns the draft mass of the entries with
+ * |p - q| <= 1e-6 * max(p, q), where that subgradient choice is arbitrary.
+ * Returns 0, or 1 (loss NaN, gradient 0) for T <= 0 or not finite, or a row
+ * whose maximum is not finite. */
+int so_overlap_grad(const void* trow, const void* drow, int dtype, int64_t V, double T, int kind, double w,
+                    double* loss, double* alpha_out, double* grad, double* tie) {
+  *loss = NAN;
+  *alpha_out = NAN;
+  *tie = 0.0;
+  for (int64_t j = 0; j < V; ++j) grad[j] = 0.0;
+  if (!(T > 0.0) || isinf(T)) return 1;
+  double* lp = (double*)malloc(sizeof(double) * (size_t)V);
+  double* lq = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!lp || !lq) { free(lp); free(lq); return 1; }
+  int bad = isnan(so_log_softmax(trow, dtype, V, T, lp)) || isnan(so_log_softmax(drow, dtype, V, T, lq));
+  if (!bad) {
+    double alpha = 0.0, beta = 0.0, tie_mass = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+      const double pj = exp(lp[j]), qj = exp(lq[j]);
+      alpha += pj < qj ? pj : qj;
+      if (qj < pj) beta += qj;
+      const double hi = pj > qj ? pj : qj;
+      if (hi > 0.0 && fabs(pj - qj) <= SO_TIE_BAND * hi) tie_mass += qj;
+    }
+    const double dl = kind == 0 ? -1.0 : -1.0 / alpha;
+    *alpha_out = alpha;
+    *loss = kind == 0 ? 1.0 - alpha : -log(alpha);
+    *tie = tie_mass;
+    for (int64_t j = 0; j < V; ++j) {
+      const double pj = exp(lp[j]), qj = exp(lq[j]);
+      grad[j] = w * dl * (qj / T) * ((qj < pj ? 1.0 : 0.0) - beta);
+    }
+  }
+  free(lp);
+  free(lq);
+  return bad;
+}
+
+/* The losses and draft-logit gradients of a batch: position i of chain b uses
+ * target row i and draft row i, weights w [B, k] (NULL: all 1).  Outputs
+ * loss, alpha, tie [B, k] and grad [B, k, V] (fp64). */
+typedef struct {
+  int64_t B, V;
+  int32_t k, dtype, kind;
+  const void* target; const void* draft; const float* T; const float* w;
+  double* loss; double* alpha; double* grad; double* tie;
+  int64_t first, stride;
+} so_grad_job;
+
+static void* grad_worker(void* arg) {
+  so_grad_job* J = (so_grad_job*)arg;
+  const size_t rs = (size_t)J->V * (J->dtype == SO_FP32 ? 4 : 2);
+  for (int64_t r = J->first; r < J->B * J->k; r += J->stride) {
+    const int64_t b = r / J->k, i = r % J->k;
+    so_overlap_grad((const char*)J->target + (size_t)(b * (J->k + 1) + i) * rs,
+                    (const char*)J->draft + (size_t)(b * J->k + i) * rs, J->dtype, J->V, (double)J->T[b], J->kind,
+                    J->w ? (double)J->w[r] : 1.0, &J->loss[r], &J->alpha[r], J->grad + (size_t)r * (size_t)J->V,
+                    &J->tie[r]);
+  }
+  return NULL;
+}
+
+int so_overlap_grad_batch(int64_t B, int32_t k, int64_t V, int32_t dtype, const void* target, const void* draft,
+                          const float* T, int32_t kind, const float* w, double* loss, double* alpha, double* grad,
+                          double* tie, int nthreads) {
+  if (B < 0 || k < 1 || V < 1 || (dtype != SO_FP32 && dtype != SO_BF16) || (kind != 0 && kind != 1)) return 1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  so_grad_job jobs[256];
+  pthread_t th[256];
+  for (int t = 0; t < nthreads; ++t)
+    jobs[t] = (so_grad_job){B, V, k, dtype, kind, target, draft, T, w, loss, alpha, grad, tie, t, nthreads};
+  if (nthreads == 1) { grad_worker(&jobs[0]); return 0; }
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, grad_worker, &jobs[t]) != 0) break;
+    started++;
+  }
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  for (int t = started; t < nthreads; ++t) grad_worker(&jobs[t]);
   return 0;
 }
 

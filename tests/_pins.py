@@ -335,6 +335,54 @@ def pin_entropy_library(orc):
         assert abs(orc.entropy(bf, T, dtype=1) - want_b) <= 1e-11 * max(1.0, want_b)
 
 
+def pin_overlap_loss_values(orc):
+    """alpha = sum min(p, q) = 1 - TV with TV = 1/2 sum |p - q| from scipy's
+    softmax; TV loss = 1 - alpha, overlap loss = -ln alpha; identical rows give
+    alpha = 1, both losses 0 and a zero gradient; invalid rows give NaN."""
+    import scipy.special
+    rng = np.random.default_rng(31)
+    for V, T in ((16, 1.0), (700, 0.6), (5000, 1.4)):
+        zt = (rng.standard_normal(V) * 2).astype(np.float32)
+        zd = (rng.standard_normal(V) * 2).astype(np.float32)
+        p = scipy.special.softmax(zt.astype(np.float64) / T)
+        q = scipy.special.softmax(zd.astype(np.float64) / T)
+        tv = 0.5 * np.abs(p - q).sum()
+        l0, a0, _, _ = orc.overlap_grad(zt, zd, T, 0)
+        l1, a1, _, _ = orc.overlap_grad(zt, zd, T, 1)
+        assert abs(a0 - (1.0 - tv)) <= 1e-12 and a0 == a1
+        assert abs(l0 - tv) <= 1e-12 and abs(l1 + math.log(1.0 - tv)) <= 1e-12
+        l, a, g, _ = orc.overlap_grad(zt, zt, T, 1)
+        assert abs(a - 1.0) <= 1e-12 and abs(l) <= 1e-12 and not np.any(g)
+    l, a, g, _ = orc.overlap_grad(np.array([0.0, np.nan], np.float32), np.zeros(2, np.float32), 1.0, 0)
+    assert math.isnan(l) and not np.any(g)
+    l, a, g, _ = orc.overlap_grad(np.zeros(3, np.float32), np.ones(3, np.float32), 0.0, 0)
+    assert math.isnan(l) and not np.any(g)
+
+
+def pin_overlap_gradient_finite_differences(orc):
+    """The gradient against central differences of the loss in every draft
+    logit (fp64 rows, away from p == q ties); it sums to zero over the row
+    (softmax invariance to a constant shift); scaling the weight scales it."""
+    rng = np.random.default_rng(37)
+    for kind in (0, 1):
+        for V, T in ((8, 1.0), (40, 0.7), (200, 1.6)):
+            zt = rng.standard_normal(V) * 1.5
+            zd = rng.standard_normal(V) * 1.5
+            loss, alpha, g, tie = orc.overlap_grad(zt, zd, T, kind, 1.0, dtype=2)
+            assert tie == 0.0
+            h = 1e-6
+            for m in range(V):
+                zp, zm = zd.copy(), zd.copy()
+                zp[m] += h
+                zm[m] -= h
+                fd = (orc.overlap_grad(zt, zp, T, kind, 1.0, dtype=2)[0] - orc.overlap_grad(zt, zm, T, kind, 1.0, dtype=2)[0]) / (2 * h)
+                assert abs(fd - g[m]) <= 1e-6 * max(1.0, abs(g[m])), (kind, V, m, fd, g[m])
+            assert abs(g.sum()) <= 1e-12 * max(1.0, np.abs(g).sum())
+            _, _, g3, _ = orc.overlap_grad(zt, zd, T, kind, 3.0, dtype=2)
+            assert np.allclose(g3, 3.0 * g, rtol=1e-14, atol=0)
+
+
 ALL_PINS = [pin_worked_examples, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
             pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact,
-            pin_entropy_closed_forms, pin_entropy_library]
+            pin_entropy_closed_forms, pin_entropy_library, pin_overlap_loss_values,
+            pin_overlap_gradient_finite_differences]

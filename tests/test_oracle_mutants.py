@@ -29,6 +29,13 @@ MUTANTS = {
     "entropy_sign_flipped": ("if (lp > -INFINITY) h -= exp(lp) * lp;", "if (lp > -INFINITY) h += exp(lp) * lp;"),
     "entropy_without_temperature": ("double lp = logit_at(row, dtype, j) / T - lse;",
                                     "double lp = logit_at(row, dtype, j) - lse;"),
+    "grad_without_temperature": ("grad[j] = w * dl * (qj / T) * ((qj < pj ? 1.0 : 0.0) - beta);",
+                                 "grad[j] = w * dl * qj * ((qj < pj ? 1.0 : 0.0) - beta);"),
+    "grad_indicator_flipped": ("grad[j] = w * dl * (qj / T) * ((qj < pj ? 1.0 : 0.0) - beta);",
+                               "grad[j] = w * dl * (qj / T) * ((qj > pj ? 1.0 : 0.0) - beta);"),
+    "grad_beta_dropped": ("grad[j] = w * dl * (qj / T) * ((qj < pj ? 1.0 : 0.0) - beta);",
+                          "grad[j] = w * dl * (qj / T) * (qj < pj ? 1.0 : 0.0);"),
+    "overlap_loss_log_missing": ("*loss = kind == 0 ? 1.0 - alpha : -log(alpha);", "*loss = kind == 0 ? 1.0 - alpha : -alpha;"),
 }
 
 
