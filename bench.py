@@ -386,6 +386,29 @@ def main(argv=None):
                                         "api": "spec_verify_ex (entropy of every target and draft row)"}
         so.close()
         del di, oo, bo
+        # training side: overlap loss and its draft-logit gradient on the same workload
+        wo = w0 if w0.batch <= 1024 else w0.scaled(batch=1024)
+        bo = si.generate(wo)
+        di = device_batch(bo, device)
+        so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16" if wo.dtype == si.BF16 else "fp32",
+                                flags=svlib.SV_FLAG_KERNEL_TIMING)
+        og = {"loss": torch.empty((wo.batch, wo.k), dtype=torch.float32, device=device), "grad": torch.empty_like(di[1])}
+        for _ in range(3):
+            so.loss_grad(di[0], di[1], di[3], kind="overlap", out=og)
+        torch.cuda.synchronize()
+        so.kernel_times()
+        for _ in range(20):
+            flush.zero_()
+            so.loss_grad(di[0], di[1], di[3], kind="overlap", out=og)
+        torch.cuda.synchronize()
+        kms = statistics.mean(so.kernel_times())
+        gb = 3 * wo.batch * wo.k * wo.vocab * (2 if wo.dtype == si.BF16 else 4)   # 2 rows read + 1 written per position
+        others[wo.name + "+loss_grad"] = {"kernel_us": 1e3 * kms, "positions_per_s": wo.batch * wo.k / (kms / 1e3),
+                                          "gbps": gb / (kms / 1e3) / 1e9, "frac_of_peak": gb / (kms / 1e3) / 1e9 / peak,
+                                          "algorithmic_bytes": gb,
+                                          "api": "spec_verify_loss_grad (overlap loss, gradient in the logit dtype)"}
+        so.close()
+        del di, og, bo
         del flush
 
     cpu = None

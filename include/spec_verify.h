@@ -109,6 +109,31 @@ int spec_verify(spec_verify_t h, int batch,
                 float* out_p_draft, float* out_q_draft, float* out_tv,
                 void* cuda_stream);
 
+/* Training-side losses on the draft-target overlap, and their gradient with
+ * respect to the draft logits (the target is frozen).  For position i of a
+ * chain (target row i, draft row i, the chain's T > 0):
+ *   alpha_i = sum_x min(p_i(x), q_i(x)) = 1 - TV_i, the probability that the
+ *   protocol accepts the drafted token ("Optimizing speculative decoding",
+ *   section "Kimi K3");
+ *   SV_LOSS_TV:      l_i = TV_i = 1 - alpha_i (section "Rejection sampling
+ *                    and a loss that optimizes acceptance directly");
+ *   SV_LOSS_OVERLAP: l_i = -ln alpha_i (section "Kimi K3").
+ * The loss is L = sum_i w_i l_i and the gradient
+ *   dL/d draft_i[m] = w_i dl/dalpha (q_i(m)/T) ([q_i(m) < p_i(m)] - beta_i),
+ *   beta_i = sum_{x: q_i(x) < p_i(x)} q_i(x),
+ * with the strict side taken at p == q (a subgradient).
+ *   weights     [batch, k] fp32 or NULL (all 1)
+ *   out_loss    [batch, k] fp32 or NULL: l_i (NaN for an invalid position)
+ *   grad_draft  [batch, k, V] in the logit dtype (bf16 rounded to nearest
+ *               even): every entry written, 0 for an invalid position
+ * A position is invalid when T is not > 0 and finite or a row has no finite
+ * maximum.  One kernel launch. */
+enum { SV_LOSS_TV = 0, SV_LOSS_OVERLAP = 1 };
+int spec_verify_loss_grad(spec_verify_t h, int batch,
+                          const void* target_logits, const void* draft_logits, const float* temperature,
+                          int loss_kind, const float* weights, float* out_loss, void* grad_draft,
+                          void* cuda_stream);
+
 /* spec_verify, and also the entropy of every logit row's distribution, in
  * the same pass over the logits.  The pages tie the fall of acceptance to
  * fluctuations in the model's output entropy, "how spread out the token

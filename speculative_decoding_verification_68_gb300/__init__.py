@@ -18,6 +18,7 @@ from . import _native
 SV_OK, SV_ERR_ARG, SV_ERR_DTYPE, SV_ERR_SIZE, SV_ERR_CUDA, SV_ERR_ALLOC, SV_ERR_DATA, SV_ERR_TIMEOUT = range(8)
 SV_FP32, SV_BF16 = 0, 1
 SV_FLAG_HOST_STAGING, SV_FLAG_NO_TMA, SV_FLAG_KERNEL_TIMING = 1, 2, 4
+SV_LOSS_TV, SV_LOSS_OVERLAP = 0, 1
 
 build = _native.build
 
@@ -137,6 +138,25 @@ class SpecVerifier:
         else:
             rc = self._lib.spec_verify(*args, self._stream(stream))
             _check(rc, "spec_verify")
+        return out
+
+    def loss_grad(self, target, draft, temperature, kind: str = "overlap", weights=None, out: dict | None = None,
+                  stream=None) -> dict:
+        """spec_verify_loss_grad: per-position loss (kind "tv": 1 - alpha, "overlap":
+        -ln alpha, alpha = sum min(p, q)) [B, k] fp32 and the gradient of the weighted
+        loss with respect to the draft logits [B, k, V] in the logit dtype."""
+        import torch
+        B = self._check_inputs(target, draft, None, temperature, None)
+        code = {"tv": SV_LOSS_TV, "overlap": SV_LOSS_OVERLAP}[kind]
+        if weights is not None:
+            assert weights.dtype == torch.float32 and tuple(weights.shape) == (B, self.k) and weights.is_contiguous()
+        if out is None:
+            out = {"loss": torch.empty((B, self.k), dtype=torch.float32, device=target.device),
+                   "grad": torch.empty_like(draft)}
+        rc = self._lib.spec_verify_loss_grad(self._h, B, _ptr(target), _ptr(draft), _ptr(temperature), code,
+                                             _ptr(weights), _ptr(out.get("loss")), _ptr(out["grad"]),
+                                             self._stream(stream))
+        _check(rc, "spec_verify_loss_grad")
         return out
 
     def verify_tv(self, target, draft, temperature, out=None, stream=None):

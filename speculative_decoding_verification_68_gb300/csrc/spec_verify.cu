@@ -90,6 +90,12 @@ struct KParams {
   int units_per_chain;       // k+1 (verify) or k (TV only)
   int tv_only;
   int tma;
+  // loss-gradient kernel
+  const float* weights;      // [B, k] or null (all 1)
+  float* out_loss;           // [B, k] or null
+  void* grad;                // [B, k, V] in the logit dtype
+  int loss_kind;             // SV_LOSS_TV or SV_LOSS_OVERLAP
+  int grad_vec;              // gradient rows can take 16-byte stores
 };
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
@@ -988,10 +994,347 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   if (lane == 0) F.out_tau[b] = tau;
 }
 
+// ------------------------------------------------------- loss-gradient kernel
+// Per position i of chain b (target row i, draft row i), from the two rows
+// held in registers:
+//   pass A and the first exchange: row statistics, as in the fused kernel;
+//   pass B: e_t = 2^(z_t c - R_t), e_d = 2^(z_d c - R_d), the indicator
+//     [q < p] = [e_t - r e_d > 0] (one bit per element, kept for pass C), and
+//     per warp B1 = sum_{q<p} e_d, B2 = sum_{q>=p} e_t;
+//   second exchange: beta = B1 / S_d, alpha = (r B1 + B2) / S_t = sum min(p, q);
+//   pass C: d(w l)/d z_d = K e_d ([q < p] - beta), K = w dl/dalpha / (T S_d),
+//     written in the logit dtype.
+// Loss: TV = 1 - alpha (SV_LOSS_TV) or -ln alpha (SV_LOSS_OVERLAP).
+
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) { u64 d; asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b)); return d; }
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// One 16-byte vector of gradients, already in the logit dtype (EPV values
+// packed in w), into the draft-gradient row `row` at slice-relative vector v;
+// entries at or past slen are not written.
+template <typename Tl>
+__device__ __forceinline__ void store_grad(void* row, int v, int slen, bool vec_ok, const uint4& w) {
+  constexpr int EPV = Lay<Tl>::EPV, ES = (int)sizeof(Tl);
+  const int e0 = v * EPV;
+  if (e0 >= slen) return;
+  if (vec_ok && e0 + EPV <= slen) {
+    reinterpret_cast<uint4*>(row)[v] = w;
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) {
+    if (e0 + e >= slen) break;
+    const uint32_t word = (e * ES) / 4 == 0 ? w.x : (e * ES) / 4 == 1 ? w.y : (e * ES) / 4 == 2 ? w.z : w.w;
+    if constexpr (ES == 4) reinterpret_cast<uint32_t*>(row)[e0 + e] = word;
+    else reinterpret_cast<uint16_t*>(row)[e0 + e] = (uint16_t)((e & 1) ? (word >> 16) : (word & 0xffffu));
+  }
+}
+// Two gradient values packed for the logit dtype: one bf16x2 word (rounded to
+// nearest even) for bf16, or the low value's bits (the caller pairs words) for fp32.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) { return bf16x2_rn(lo, hi); }
+
+// Sum of 32-byte exchange items l and l + 32 over the warp, for the s_t and s_d fields.
+__device__ __forceinline__ void warp_sum_items(const X1* it, int items, float& a, float& d) {
+  const int lane = threadIdx.x & 31;
+  float a0 = lane < items ? it[lane].s_t : 0.0f, d0 = lane < items ? it[lane].s_d : 0.0f;
+  float a1 = lane + 32 < items ? it[lane + 32].s_t : 0.0f, d1 = lane + 32 < items ? it[lane + 32].s_d : 0.0f;
+  u64 v = add2(pk(a0, d0), pk(a1, d1));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float x, y;
+    upk(v, x, y);
+    v = add2(v, pk(__shfl_xor_sync(FULL, x, o), __shfl_xor_sync(FULL, y, o)));
+  }
+  upk(v, a, d);
+}
+
+// A scheduling fence between vectors: the next vector's registers are made to
+// depend on the accumulator, so the compiler keeps one vector in flight per
+// thread instead of hoisting every exponential of the unrolled loop (which
+// spills at 128 registers).
+__device__ __forceinline__ void fence_vec(uint4& a, uint4& b, u64& acc) {
+  asm volatile("" : "+r"(a.x), "+r"(a.y), "+r"(a.z), "+r"(a.w), "+r"(b.x), "+r"(b.y), "+r"(b.z), "+r"(b.w), "+l"(acc));
+}
+
+struct alignas(16) GradStat {   // the second merge, published by warp 0
+  float beta, K;
+  int ok, pad;
+};
+
+template <typename Tl, int R>
+__device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* gs, const uint4* blk_t,
+                                          const uint4* blk_d, const Geo& g, const Unit un, unsigned phase, int& n1,
+                                          const uint32_t bar, const unsigned char* smem_stage, const Unit next,
+                                          bool tma_next, const float T) {
+  constexpr int EPV = Lay<Tl>::EPV;
+  constexpr int ES = (int)sizeof(Tl);
+  constexpr int NBW = (R * EPV + 31) / 32;   // indicator words per thread
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k, V = P.V;
+  const int b = un.b, ipos = un.ipos;
+  const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
+
+  uint4 rt[R], rd[R];
+  if (P.tma) {
+    mbar_wait_bounded(bar, phase, P.flags);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      rt[j] = blk_t[j * 32 + lane];
+      rd[j] = blk_d[j * 32 + lane];
+    }
+    __syncwarp();
+    bool last = false;
+    if (lane == 0) last = stage_release_last(&S.cnt);
+    last = __shfl_sync(FULL, last, 0);
+    if (last && tma_next) issue_unit_load<Tl, R>(P, g, next, bar, smem_stage);
+  } else {
+    const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0()) * ES;
+    const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0()) * ES;
+    const int nv = nvec_of<Tl>(g), vb = g.vbeg(), ve = min(vb + P.wv, nv);
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int v = vb + j * 32 + lane;
+      rt[j] = load_vec_direct<Tl>(tb, v, g.slen(), v < ve);
+      rd[j] = load_vec_direct<Tl>(db, v, g.slen(), v < ve);
+    }
+  }
+
+  const bool t_ok = T > 0.0f && T <= 3.0e38f;   // the losses need a sampling temperature
+  const float c = t_ok ? fminf(__fdiv_rn(LOG2E_F, T), 3.0e38f) : 0.0f;
+
+  // ---------------- pass A and the first exchange: row statistics
+  MaxAcc<Tl> mx_t, mx_d;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    mx_t.add(rt[j]);
+    mx_d.add(rd[j]);
+  }
+  X1 mine;
+  mine.m_t = warp_max_nan(mx_t.get());
+  mine.m_d = warp_max_nan(mx_d.get());
+  mine.i_t = 0; mine.i_d = 0;
+  const u64 cc = pk(c, c);
+  mine.ref_t = iref_of(mine.m_t, c);
+  mine.ref_d = iref_of(mine.m_d, c);
+  {
+    const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
+    const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
+    mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
+    mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+  }
+  const int item = g.rank() * NWARP + warp;
+  {
+    const int set1 = n1 & 1;
+    const uint32_t xbar = saddr(&S.xbar[set1]);
+    if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items() * 32u);
+    if (lane < (int)g.C()) st_async_x1(peer_addr(saddr(&S.x1[set1][item]), lane), mine, peer_addr(xbar, lane));
+    const unsigned xpar = (unsigned)((n1 >> 1) & 1);
+    ++n1;
+    Merged& mg = S.mg[set1];
+    if (warp == 0) {
+      mbar_wait_cluster_bounded(xbar, xpar, P.flags);
+      X1 z;
+      z.m_t = -INFINITY; z.m_d = -INFINITY; z.s_t = 0.0f; z.s_d = 0.0f; z.i_t = 0; z.i_d = 0;
+      z.ref_t = NO_REF; z.ref_d = NO_REF;
+      const X1 ia = lane < g.items() ? S.x1[set1][lane] : z;
+      const X1 ib = lane + 32 < g.items() ? S.x1[set1][lane + 32] : z;
+      const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t)), M_d = warp_max_nan(nanmax(ia.m_d, ib.m_d));
+      const int IR_t = warp_max_s32(max(ia.ref_t, ib.ref_t)), IR_d = warp_max_s32(max(ia.ref_d, ib.ref_d));
+      u64 st = add2(pk(ia.s_t * pow2_diff(ia.ref_t, IR_t), ia.s_d * pow2_diff(ia.ref_d, IR_d)),
+                    pk(ib.s_t * pow2_diff(ib.ref_t, IR_t), ib.s_d * pow2_diff(ib.ref_d, IR_d)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float x, y;
+        upk(st, x, y);
+        st = add2(st, pk(__shfl_xor_sync(FULL, x, o), __shfl_xor_sync(FULL, y, o)));
+      }
+      float S_t, S_d;
+      upk(st, S_t, S_d);
+      const bool row_ok = t_ok && isfinite(M_t) && isfinite(M_d) && fabsf(M_t * c) < REF_LIMIT &&
+                          fabsf(M_d * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t) && S_d > 0.0f && isfinite(S_d);
+      if (lane == 0) {
+        Merged m;
+        m.S_t = S_t; m.S_d = S_d;
+        m.R_t = IR_t == NO_REF ? 0.0f : (float)IR_t; m.R_d = IR_d == NO_REF ? 0.0f : (float)IR_d;
+        m.r = row_ok ? S_t / S_d : 0.0f; m.IR_t = IR_t; m.status = row_ok ? 0 : ST_ROW; m.pad = 0;
+        mg = m;
+      }
+      __syncwarp();
+      merged_arrive();
+    } else {
+      merged_wait();
+    }
+  }
+  const Merged M = S.mg[(n1 - 1) & 1];
+  char* grow = (char*)P.grad + ((size_t)drow * V + g.slice0()) * ES;
+  const int slen = g.slen(), vb = g.vbeg();
+  if (M.status != 0) {   // invalid position: zero gradient, NaN loss
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (j * 32 + lane < P.wv) store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(0u, 0u, 0u, 0u));
+    if (tid == 0 && g.rank() == 0 && P.out_loss) P.out_loss[(size_t)b * k + ipos] = __int_as_float(0x7fc00000);
+    return;
+  }
+
+  // ---------------- pass B: indicator bits and the two masses of this warp's range
+  const u64 nrt = pk(-M.R_t, -M.R_t), nrd = pk(-M.R_d, -M.R_d), nr = pk(-M.r, -M.r);
+  unsigned bits[NBW];
+#pragma unroll
+  for (int q = 0; q < NBW; ++q) bits[q] = 0u;
+  u64 b1 = 0ull, b2 = 0ull;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+#pragma unroll
+    for (int e = 0; e < EPV; e += 2) {
+      const float t0 = Lay<Tl>::elem(rt[j], e), t1 = Lay<Tl>::elem(rt[j], e + 1);
+      const float d0 = Lay<Tl>::elem(rd[j], e), d1 = Lay<Tl>::elem(rd[j], e + 1);
+      float at0, at1, ad0, ad1;
+      upk(fma2(pk(t0, t1), cc, nrt), at0, at1);
+      upk(fma2(pk(d0, d1), cc, nrd), ad0, ad1);
+      const float et0 = ex2(at0), et1 = ex2(at1), ed0 = ex2(ad0), ed1 = ex2(ad1);
+      float y0, y1;
+      upk(fma2(pk(ed0, ed1), nr, pk(et0, et1)), y0, y1);   // e_t - r e_d: > 0 exactly when q < p
+      const bool i0 = y0 > 0.0f, i1 = y1 > 0.0f;
+      const int pos = j * EPV + e;
+      bits[pos >> 5] |= (i0 ? 1u : 0u) << (pos & 31);
+      bits[(pos + 1) >> 5] |= (i1 ? 1u : 0u) << ((pos + 1) & 31);
+      b1 = add2(b1, pk(i0 ? ed0 : 0.0f, i1 ? ed1 : 0.0f));
+      b2 = add2(b2, pk(i0 ? 0.0f : et0, i1 ? 0.0f : et1));
+    }
+    if (j + 1 < R) fence_vec(rt[j + 1], rd[j + 1], b1);
+  }
+  X1 m2;
+  {
+    float x, y;
+    upk(b1, x, y);
+    m2.s_t = warp_sum_f32(x + y);
+    upk(b2, x, y);
+    m2.s_d = warp_sum_f32(x + y);
+  }
+  m2.m_t = 0.0f; m2.m_d = 0.0f; m2.i_t = 0; m2.i_d = 0; m2.ref_t = 0; m2.ref_d = 0;
+  {
+    const int set2 = n1 & 1;
+    const uint32_t xbar = saddr(&S.xbar[set2]);
+    if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items() * 32u);
+    if (lane < (int)g.C()) st_async_x1(peer_addr(saddr(&S.x1[set2][item]), lane), m2, peer_addr(xbar, lane));
+    const unsigned xpar = (unsigned)((n1 >> 1) & 1);
+    ++n1;
+    GradStat& gst = gs[set2];
+    if (warp == 0) {
+      mbar_wait_cluster_bounded(xbar, xpar, P.flags);
+      float B1, B2;
+      warp_sum_items(S.x1[set2], g.items(), B1, B2);
+      const float beta = B1 / M.S_d;
+      const float alpha = fmaf(M.r, B1, B2) / M.S_t;
+      const int kind = P.loss_kind;
+      const float w = P.weights ? P.weights[(size_t)b * k + ipos] : 1.0f;
+      const float dl = kind == 0 ? -1.0f : -1.0f / alpha;
+      if (lane == 0) {
+        GradStat gv;
+        gv.beta = beta;
+        gv.K = w * dl / (T * M.S_d);
+        gv.ok = 1; gv.pad = 0;
+        gst = gv;
+        if (g.rank() == 0 && P.out_loss) P.out_loss[(size_t)b * k + ipos] = kind == 0 ? 1.0f - alpha : -logf(alpha);
+      }
+      __syncwarp();
+      merged_arrive();
+    } else {
+      merged_wait();
+    }
+  }
+  const GradStat G = gs[(n1 - 1) & 1];
+
+  // ---------------- pass C: the gradient of this warp's range of the draft row
+  const float sel1 = G.K * (1.0f - G.beta), sel0 = -G.K * G.beta;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    uint32_t wd[4];
+#pragma unroll
+    for (int e = 0; e < EPV; e += 2) {
+      float ad0, ad1;
+      upk(fma2(pk(Lay<Tl>::elem(rd[j], e), Lay<Tl>::elem(rd[j], e + 1)), cc, nrd), ad0, ad1);
+      const int pos = j * EPV + e;
+      const float s0 = (bits[pos >> 5] >> (pos & 31)) & 1u ? sel1 : sel0;
+      const float s1 = (bits[(pos + 1) >> 5] >> ((pos + 1) & 31)) & 1u ? sel1 : sel0;
+      float g0, g1;
+      upk(mul2(pk(ex2(ad0), ex2(ad1)), pk(s0, s1)), g0, g1);
+      if constexpr (sizeof(Tl) == 4) { wd[e] = __float_as_uint(g0); wd[e + 1] = __float_as_uint(g1); }
+      else wd[e >> 1] = pack_bf16x2(g0, g1);
+    }
+    if (j * 32 + lane < P.wv)
+      store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+    if (j + 1 < R) {
+      u64 dep = pk(__uint_as_float(wd[0]), __uint_as_float(wd[1]));
+      fence_vec(rt[j + 1], rd[j + 1], dep);
+    }
+  }
+}
+
+template <typename Tl, int R>
+__global__ void __launch_bounds__(NT, 2) sv_grad_kernel(const KParams P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ GradStat gs[2];
+  Small& S = *reinterpret_cast<Small*>(smem);
+  unsigned char* stage = smem + SMALL_BYTES;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  Geo g;
+  g.p = &P;
+  const unsigned cid = cl_id(), ncl = cl_count();
+  const unsigned B = (unsigned)P.B;
+  const unsigned n_units = B * (unsigned)P.k;   // positions; below 2^31 (checked on the host)
+  const uint32_t bar = saddr(&S.bar);
+  const uint4* blk_t = reinterpret_cast<const uint4*>(stage) + (size_t)(0 * NWARP + warp) * R * 32;
+  const uint4* blk_d = reinterpret_cast<const uint4*>(stage) + (size_t)(1 * NWARP + warp) * R * 32;
+  if (P.tma) {
+    uint4* st = reinterpret_cast<uint4*>(stage);
+    for (int i = tid; i < 2 * NWARP * R * 32; i += NT) st[i] = Lay<Tl>::neg_inf();
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init(saddr(&S.xbar[0]), 1);
+    mbar_init(saddr(&S.xbar[1]), 1);
+    S.cnt = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  cluster_sync_all();
+  unsigned u = cid;
+  Unit cur = unit_of(u, B);
+  if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+  unsigned phase = 0;
+  int n1 = 0;
+  for (; u < n_units; u += ncl, phase ^= 1u) {
+    const bool has_next = u + ncl < n_units;
+    const Unit next = unit_of(u + ncl, B);
+    grad_unit<Tl, R>(P, S, gs, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && has_next,
+                     P.temperature[cur.b]);
+    cur = next;
+  }
+  cluster_sync_all();
+}
+
 typedef void (*FusedFn)(const KParams);
 typedef void (*FinalFn)(const FParams);
 constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10};
 constexpr int N_R = 6;
+
+template <typename Tl>
+FusedFn pick_grad(int r) {
+  switch (r) {
+    case 1: return sv_grad_kernel<Tl, 1>;
+    case 2: return sv_grad_kernel<Tl, 2>;
+    case 4: return sv_grad_kernel<Tl, 4>;
+    case 6: return sv_grad_kernel<Tl, 6>;
+    case 8: return sv_grad_kernel<Tl, 8>;
+    default: return sv_grad_kernel<Tl, 10>;
+  }
+}
 
 template <typename Tl>
 void pick_kernels(int r, FusedFn& f, FusedFn& fe, FinalFn& g) {
@@ -1017,6 +1360,8 @@ struct spec_verify_ctx {
   FusedFn kernel;
   FusedFn kernel_ent;        // the same kernel that also writes row entropies
   int n_clusters_ent;
+  FusedFn kernel_grad;       // loss-gradient kernel
+  int n_clusters_grad;
   FinalFn finalize;
   int32_t* ws_acc;
   int32_t* ws_y;
@@ -1056,9 +1401,9 @@ static void free_ctx(spec_verify_ctx* h) {
   free(h);
 }
 
-static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s) {
+static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s, bool grad = false) {
   const bool ent = P.out_ent_t || P.out_ent_d;
-  const int ncl = ent ? h->n_clusters_ent : h->n_clusters;
+  const int ncl = grad ? h->n_clusters_grad : ent ? h->n_clusters_ent : h->n_clusters;
   const int grid_clusters = (int)(units < ncl ? units : ncl);
   if (grid_clusters <= 0) return SV_OK;
   const bool timed = h->ev && h->ev_n < TIMING_RING;
@@ -1076,7 +1421,8 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, ent ? h->kernel_ent : h->kernel, P) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : ent ? h->kernel_ent : h->kernel, P) != cudaSuccess)
+    return SV_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(h->ev[2 * h->ev_n + 1], s) != cudaSuccess) return SV_ERR_CUDA;
     h->ev_n++;
@@ -1257,8 +1603,10 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   h->smem = SMALL_BYTES + (h->tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
   if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->finalize);
   else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->finalize);
+  h->kernel_grad = logit_dtype == SV_FP32 ? pick_grad<float>(R) : pick_grad<__nv_bfloat16>(R);
   if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
-      cudaFuncSetAttribute(h->kernel_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
+      cudaFuncSetAttribute(h->kernel_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
+      cudaFuncSetAttribute(h->kernel_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
     free_ctx(h);
     return SV_ERR_CUDA;
   }
@@ -1275,15 +1623,17 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0, ne = 0;
+    int n = 0, ne = 0, ng = 0;
     if (cudaOccupancyMaxActiveClusters(&n, h->kernel, &cfg) != cudaSuccess || n <= 0 ||
-        cudaOccupancyMaxActiveClusters(&ne, h->kernel_ent, &cfg) != cudaSuccess || ne <= 0) {
+        cudaOccupancyMaxActiveClusters(&ne, h->kernel_ent, &cfg) != cudaSuccess || ne <= 0 ||
+        cudaOccupancyMaxActiveClusters(&ng, h->kernel_grad, &cfg) != cudaSuccess || ng <= 0) {
       cudaGetLastError();
       free_ctx(h);
       return SV_ERR_CUDA;
     }
     h->n_clusters = n;
     h->n_clusters_ent = ne;
+    h->n_clusters_grad = ng;
   }
   const size_t mb = (size_t)(max_batch > 0 ? max_batch : 1);
   bool ok = cudaMalloc(&h->ws_acc, mb * k * sizeof(int32_t)) == cudaSuccess &&
@@ -1441,6 +1791,28 @@ int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const 
   int rc = launch_fused(h, P, (long long)batch * h->k, s);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, nullptr, nullptr, nullptr, s);
+}
+
+int spec_verify_loss_grad(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                          const float* temperature, int loss_kind, const float* weights, float* out_loss,
+                          void* grad_draft, void* cuda_stream) {
+  if (!h || batch < 0 || batch > h->max_batch) return SV_ERR_ARG;
+  if (loss_kind != SV_LOSS_TV && loss_kind != SV_LOSS_OVERLAP) return SV_ERR_ARG;
+  if (batch == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !temperature || !grad_draft) return SV_ERR_ARG;
+  const int es = h->dtype == SV_FP32 ? 4 : 2;
+  if (((uintptr_t)target_logits % es) || ((uintptr_t)draft_logits % es) || ((uintptr_t)grad_draft % es)) return SV_ERR_ARG;
+  if (!al4(temperature) || !al4(weights) || !al4(out_loss)) return SV_ERR_ARG;
+  KParams P;
+  memset(&P, 0, sizeof P);
+  P.target = target_logits; P.draft = draft_logits; P.temperature = temperature;
+  P.weights = weights; P.out_loss = out_loss; P.grad = grad_draft; P.loss_kind = loss_kind;
+  P.flags = h->d_flags;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.units_per_chain = h->k; P.tv_only = 1;
+  P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.grad_vec = ((size_t)h->V * es) % 16 == 0 && al16(grad_draft);
+  return launch_fused(h, P, (long long)batch * h->k, (cudaStream_t)cuda_stream, true);
 }
 
 int spec_verify_host(spec_verify_t h, int batch, const void* host_target_logits, const void* host_draft_logits,
