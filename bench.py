@@ -386,6 +386,30 @@ def main(argv=None):
                                         "api": "spec_verify_ex (entropy of every target and draft row)"}
         so.close()
         del di, oo, bo
+        # lazy verification (no TV) on the workloads without TV: whole call timed with events
+        for wo in (si.C3_T1, si.C4):
+            bo = si.generate(wo)
+            di = device_batch(bo, device)
+            so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16" if wo.dtype == si.BF16 else "fp32")
+            ol = so.alloc_outputs(wo.batch, want_pq=False, device=device)
+            for _ in range(3):
+                so.verify_lazy(*di, out=ol)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for _ in range(20):
+                flush.zero_()
+                ev0.record()
+                so.verify_lazy(*di, out=ol)
+                ev1.record()
+                torch.cuda.synchronize()
+                tot += ev0.elapsed_time(ev1)
+            ms = tot / 20
+            others[wo.name + "+lazy"] = {"call_us": 1e3 * ms, "draft_tokens_per_s": wo.batch * wo.k / (ms / 1e3),
+                                         "chains_per_s": wo.batch / (ms / 1e3), "mean_tau": float(ol["tau"].float().mean().item()),
+                                         "launches_per_call": wo.k + 2,
+                                         "api": "spec_verify_lazy (rows past the first rejection are not read; whole call)"}
+            so.close()
+            del di, ol, bo
         # training side: overlap loss and its draft-logit gradient on the same workload
         wo = w0 if w0.batch <= 1024 else w0.scaled(batch=1024)
         bo = si.generate(wo)

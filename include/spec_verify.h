@@ -109,6 +109,21 @@ int spec_verify(spec_verify_t h, int batch,
                 float* out_p_draft, float* out_q_draft, float* out_tv,
                 void* cuda_stream);
 
+/* Lazy verification: the same protocol, verifying positions in order and
+ * reading no logit row past a chain's first rejection (the protocol stops
+ * there: "Optimizing speculative decoding", section "The draft model moved
+ * inside", and "DSpark for GLM-5.2", introduction).  out_tokens and out_tau
+ * are bit-identical to spec_verify's for every chain whose rows up to its
+ * stop are valid; a chain is invalid (tau = -1) only if a row it reads is
+ * (rows after the stop are never read, so their contents do not matter).
+ * There is no p, q or TV output (positions after the stop are not
+ * evaluated).  k + 2 kernel launches: one per position 0..k, each over the
+ * chains still verifying, then the finalize kernel. */
+int spec_verify_lazy(spec_verify_t h, int batch,
+                     const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                     int32_t* out_tokens, int32_t* out_tau, void* cuda_stream);
+
 /* Training-side losses on the draft-target overlap, and their gradient with
  * respect to the draft logits (the target is frozen).  For position i of a
  * chain (target row i, draft row i, the chain's T > 0):

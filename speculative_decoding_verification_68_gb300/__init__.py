@@ -140,6 +140,17 @@ class SpecVerifier:
             _check(rc, "spec_verify")
         return out
 
+    def verify_lazy(self, target, draft, tokens, temperature, uniforms, out: dict | None = None, stream=None) -> dict:
+        """spec_verify_lazy: verification that reads no row past a chain's first
+        rejection (tokens and tau only; no p, q or TV)."""
+        B = self._check_inputs(target, draft, tokens, temperature, uniforms)
+        if out is None:
+            out = self.alloc_outputs(B, want_pq=False, want_tv=False, device=target.device)
+        rc = self._lib.spec_verify_lazy(self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature),
+                                        _ptr(uniforms), _ptr(out["tokens"]), _ptr(out["tau"]), self._stream(stream))
+        _check(rc, "spec_verify_lazy")
+        return out
+
     def loss_grad(self, target, draft, temperature, kind: str = "overlap", weights=None, out: dict | None = None,
                   stream=None) -> dict:
         """spec_verify_loss_grad: per-position loss (kind "tv": 1 - alpha, "overlap":

@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_init.argtypes = [p(vp), i, i, i, i, u]
     lib.spec_verify.restype = i
     lib.spec_verify.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_lazy.restype = i
+    lib.spec_verify_lazy.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_loss_grad.restype = i
     lib.spec_verify_loss_grad.argtypes = [vp, i, vp, vp, vp, i, vp, vp, vp, vp]
     lib.spec_verify_ex.restype = i

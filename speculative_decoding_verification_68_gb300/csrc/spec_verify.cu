@@ -96,7 +96,11 @@ struct KParams {
   void* grad;                // [B, k, V] in the logit dtype
   int loss_kind;             // SV_LOSS_TV or SV_LOSS_OVERLAP
   int grad_vec;              // gradient rows can take 16-byte stores
+  // lazy verification (one launch per position)
+  int lazy_pos;              // the position this launch verifies
+  int* ws_next;              // [B] the next position a chain waits for (LAZY_DONE: stopped)
 };
+constexpr int LAZY_DONE = 0x7fffffff;
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
   float m_t, m_d;              // maxima of the warp's range in the target / draft row
@@ -496,7 +500,7 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
 __device__ __forceinline__ void merged_arrive() { asm volatile("bar.arrive 1, %0;" ::"n"(NT) : "memory"); }
 __device__ __forceinline__ void merged_wait() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
-template <typename Tl, int R, bool PAIR, bool ENT>
+template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
 __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
@@ -710,7 +714,12 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
               P.ws_acc[pi] = x == A_t;
               if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
               if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
+              if (LAZY) P.ws_next[b] = x == A_t ? ipos + 1 : LAZY_DONE;
             }
+          }
+          if (LAZY && PAIR && status != 0) {   // an invalid position stops the chain
+            P.ws_acc[pi] = 0;
+            P.ws_next[b] = LAZY_DONE;
           }
           if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
         }
@@ -750,12 +759,13 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     const float ratio = exp2f(lpx - lqx) * (M.S_d / M.S_t);
     const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
     P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
+    if (LAZY) P.ws_next[b] = u_acc < ratio ? ipos + 1 : LAZY_DONE;
     if (P.out_p) P.out_p[pi] = exp2f(lpx) / M.S_t;
     if (P.out_q) P.out_q[pi] = exp2f(lqx) / M.S_d;
   }
 }
 
-template <typename Tl, int R, bool ENT>
+template <typename Tl, int R, bool ENT, bool LAZY>
 __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   Small& S = *reinterpret_cast<Small*>(smem);
@@ -787,24 +797,52 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   __syncthreads();
   cluster_sync_all();   // every peer's shared memory is live before the first remote store
 
-  unsigned u = cid;
-  Unit cur = unit_of(u, B);
-  if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
-  // Per-unit scalars (temperature, drafted token) are loaded one unit ahead,
-  // so their latency is hidden behind a whole unit of work.
-  for (; u < n_units; u += ncl, phase ^= 1u) {
-    const bool has_next = u + ncl < n_units;
-    const Unit next = unit_of(u + ncl, B);
-    const float T = P.temperature[cur.b];
-    const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
-    const bool tma_next = P.tma && has_next;
-    if (cur.ipos < k)
-      process_unit<Tl, R, true, ENT>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
-    else
-      process_unit<Tl, R, false, ENT>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
-    cur = next;
+  if constexpr (LAZY) {
+    // One position for every chain still verifying at it: the chains this
+    // cluster owns (b = cluster_id mod n_clusters) whose next position is
+    // P.lazy_pos.  A chain's flag is written only after the cluster has
+    // exchanged that chain's statistics, by which time every CTA of the
+    // cluster has read it, so all CTAs walk the same chains.
+    const int pos = P.lazy_pos;
+    auto waiting = [&](unsigned bb) { return pos == 0 || __ldcg(&P.ws_next[bb]) == pos; };
+    unsigned u = cid;
+    while (u < B && !waiting(u)) u += ncl;
+    Unit cur;
+    cur.b = (int)u; cur.ipos = pos;
+    if (P.tma && warp == 0 && u < B) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+    while (u < B) {
+      unsigned un = u + ncl;
+      while (un < B && !waiting(un)) un += ncl;
+      Unit next;
+      next.b = (int)un; next.ipos = pos;
+      const float T = P.temperature[cur.b];
+      const int x = pos < k ? P.tokens[(size_t)cur.b * k + pos] : 0;
+      if (pos < k)
+        process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && un < B, T, x);
+      else
+        process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && un < B, T, x);
+      cur = next;
+      u = un;
+      phase ^= 1u;
+    }
+  } else {
+    unsigned u = cid;
+    Unit cur = unit_of(u, B);
+    if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+    for (; u < n_units; u += ncl, phase ^= 1u) {
+      const bool has_next = u + ncl < n_units;
+      const Unit next = unit_of(u + ncl, B);
+      const float T = P.temperature[cur.b];
+      const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
+      const bool tma_next = P.tma && has_next;
+      if (cur.ipos < k)
+        process_unit<Tl, R, true, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+      else
+        process_unit<Tl, R, false, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+      cur = next;
+    }
   }
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
 }
@@ -825,6 +863,7 @@ struct FParams {
   float* out_tv;
   int* flags;
   int B, k, V, Vs, wv, items, tma, tv_only;
+  int lazy;   // positions after the first rejection were not verified
 };
 
 // One warp per chain: tau by ballot, TV from the per-range masses, and the
@@ -839,7 +878,13 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   const int k = F.k, items = F.items;
   const size_t ub = (size_t)b * (k + 1);
   const int npos = F.tv_only ? k : k + 1;
-  const int st = lane < npos ? F.ws_stat[ub + lane].status : 0;
+  int last = npos - 1;   // the last position whose unit was verified
+  if (F.lazy) {          // only positions up to the first rejection were: find it first
+    const int a0 = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
+    const unsigned rej0 = __ballot_sync(FULL, lane < k && a0 == 0);
+    last = rej0 ? __ffs(rej0) - 1 : k;
+  }
+  const int st = lane < npos && lane <= last ? F.ws_stat[ub + lane].status : 0;
   const bool bad = __any_sync(FULL, st != 0);
 
   // TV of every valid, non-greedy position
@@ -1336,15 +1381,22 @@ FusedFn pick_grad(int r) {
   }
 }
 
+template <typename Tl, int R>
+void pick_r(FusedFn& f, FusedFn& fe, FusedFn& fl, FinalFn& g) {
+  f = sv_fused_kernel<Tl, R, false, false>;
+  fe = sv_fused_kernel<Tl, R, true, false>;
+  fl = sv_fused_kernel<Tl, R, false, true>;
+  g = sv_finalize_kernel<Tl, R>;
+}
 template <typename Tl>
-void pick_kernels(int r, FusedFn& f, FusedFn& fe, FinalFn& g) {
+void pick_kernels(int r, FusedFn& f, FusedFn& fe, FusedFn& fl, FinalFn& g) {
   switch (r) {
-    case 1: f = sv_fused_kernel<Tl, 1, false>; fe = sv_fused_kernel<Tl, 1, true>; g = sv_finalize_kernel<Tl, 1>; break;
-    case 2: f = sv_fused_kernel<Tl, 2, false>; fe = sv_fused_kernel<Tl, 2, true>; g = sv_finalize_kernel<Tl, 2>; break;
-    case 4: f = sv_fused_kernel<Tl, 4, false>; fe = sv_fused_kernel<Tl, 4, true>; g = sv_finalize_kernel<Tl, 4>; break;
-    case 6: f = sv_fused_kernel<Tl, 6, false>; fe = sv_fused_kernel<Tl, 6, true>; g = sv_finalize_kernel<Tl, 6>; break;
-    case 8: f = sv_fused_kernel<Tl, 8, false>; fe = sv_fused_kernel<Tl, 8, true>; g = sv_finalize_kernel<Tl, 8>; break;
-    default: f = sv_fused_kernel<Tl, 10, false>; fe = sv_fused_kernel<Tl, 10, true>; g = sv_finalize_kernel<Tl, 10>; break;
+    case 1: pick_r<Tl, 1>(f, fe, fl, g); break;
+    case 2: pick_r<Tl, 2>(f, fe, fl, g); break;
+    case 4: pick_r<Tl, 4>(f, fe, fl, g); break;
+    case 6: pick_r<Tl, 6>(f, fe, fl, g); break;
+    case 8: pick_r<Tl, 8>(f, fe, fl, g); break;
+    default: pick_r<Tl, 10>(f, fe, fl, g); break;
   }
 }
 
@@ -1362,6 +1414,9 @@ struct spec_verify_ctx {
   int n_clusters_ent;
   FusedFn kernel_grad;       // loss-gradient kernel
   int n_clusters_grad;
+  FusedFn kernel_lazy;       // one position of lazy verification
+  int n_clusters_lazy;
+  int* ws_next;              // [max_batch] next position of each chain (lazy)
   FinalFn finalize;
   int32_t* ws_acc;
   int32_t* ws_y;
@@ -1389,7 +1444,7 @@ static constexpr int TIMING_RING = 4096;
 
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
-  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
+  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->ws_next, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
                   h->st_unif, h->st_out_tokens, h->st_out_tau, h->st_out_p, h->st_out_q, h->st_out_tv};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -1401,9 +1456,10 @@ static void free_ctx(spec_verify_ctx* h) {
   free(h);
 }
 
-static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s, bool grad = false) {
+static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s, bool grad = false,
+                        bool lazy = false) {
   const bool ent = P.out_ent_t || P.out_ent_d;
-  const int ncl = grad ? h->n_clusters_grad : ent ? h->n_clusters_ent : h->n_clusters;
+  const int ncl = grad ? h->n_clusters_grad : lazy ? h->n_clusters_lazy : ent ? h->n_clusters_ent : h->n_clusters;
   const int grid_clusters = (int)(units < ncl ? units : ncl);
   if (grid_clusters <= 0) return SV_OK;
   const bool timed = h->ev && h->ev_n < TIMING_RING;
@@ -1421,7 +1477,8 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : ent ? h->kernel_ent : h->kernel, P) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : lazy ? h->kernel_lazy : ent ? h->kernel_ent : h->kernel, P) !=
+      cudaSuccess)
     return SV_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(h->ev[2 * h->ev_n + 1], s) != cudaSuccess) return SV_ERR_CUDA;
@@ -1431,7 +1488,7 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
 }
 
 static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* tokens, int32_t* out_tokens,
-                           int32_t* out_tau, cudaStream_t s) {
+                           int32_t* out_tau, cudaStream_t s, bool lazy = false) {
   FParams F;
   memset(&F, 0, sizeof F);
   F.target = P.target; F.draft = P.draft; F.tokens = tokens; F.uniforms = P.uniforms;
@@ -1439,6 +1496,7 @@ static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* 
   F.out_tokens = out_tokens; F.out_tau = out_tau; F.out_tv = P.out_tv; F.flags = P.flags;
   F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.wv = P.wv; F.items = h->C * NWARP; F.tma = P.tma;
   F.tv_only = P.tv_only;
+  F.lazy = lazy ? 1 : 0;
   h->finalize<<<(P.B + 7) / 8, 256, 0, s>>>(F);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
@@ -1518,8 +1576,8 @@ int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) 
   h.C = C; h.Vs = (int)Vs; h.R = R; h.wv = (int)wv;
   h.tma_ok = ((size_t)vocab * es) % 16 == 0;
   h.smem = SMALL_BYTES + (h.tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
-  if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.finalize);
-  else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.finalize);
+  if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
+  else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
   if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem) != cudaSuccess)
     return SV_ERR_CUDA;
   cudaLaunchConfig_t cfg;
@@ -1601,12 +1659,13 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   h->C = C; h->Vs = (int)Vs; h->R = R; h->wv = (int)wv;
   h->tma_ok = ((size_t)vocab * es) % 16 == 0 && !(flags & SV_FLAG_NO_TMA);
   h->smem = SMALL_BYTES + (h->tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
-  if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->finalize);
-  else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->finalize);
+  if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
+  else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
   h->kernel_grad = logit_dtype == SV_FP32 ? pick_grad<float>(R) : pick_grad<__nv_bfloat16>(R);
   if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
       cudaFuncSetAttribute(h->kernel_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
-      cudaFuncSetAttribute(h->kernel_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
+      cudaFuncSetAttribute(h->kernel_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
+      cudaFuncSetAttribute(h->kernel_lazy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
     free_ctx(h);
     return SV_ERR_CUDA;
   }
@@ -1623,10 +1682,11 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0, ne = 0, ng = 0;
+    int n = 0, ne = 0, ng = 0, nl = 0;
     if (cudaOccupancyMaxActiveClusters(&n, h->kernel, &cfg) != cudaSuccess || n <= 0 ||
         cudaOccupancyMaxActiveClusters(&ne, h->kernel_ent, &cfg) != cudaSuccess || ne <= 0 ||
-        cudaOccupancyMaxActiveClusters(&ng, h->kernel_grad, &cfg) != cudaSuccess || ng <= 0) {
+        cudaOccupancyMaxActiveClusters(&ng, h->kernel_grad, &cfg) != cudaSuccess || ng <= 0 ||
+        cudaOccupancyMaxActiveClusters(&nl, h->kernel_lazy, &cfg) != cudaSuccess || nl <= 0) {
       cudaGetLastError();
       free_ctx(h);
       return SV_ERR_CUDA;
@@ -1634,6 +1694,7 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     h->n_clusters = n;
     h->n_clusters_ent = ne;
     h->n_clusters_grad = ng;
+    h->n_clusters_lazy = nl;
   }
   const size_t mb = (size_t)(max_batch > 0 ? max_batch : 1);
   bool ok = cudaMalloc(&h->ws_acc, mb * k * sizeof(int32_t)) == cudaSuccess &&
@@ -1641,7 +1702,8 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
             cudaMalloc(&h->ws_stat, mb * (k + 1) * sizeof(UnitStat)) == cudaSuccess &&
             cudaMalloc(&h->ws_w, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->ws_p, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess;
+            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&h->ws_next, mb * sizeof(int)) == cudaSuccess;
   if (ok && (flags & SV_FLAG_HOST_STAGING)) {
     const size_t rowb = (size_t)vocab * es;
     ok = cudaMalloc(&h->st_target, mb * (k + 1) * rowb) == cudaSuccess &&
@@ -1713,6 +1775,35 @@ int spec_verify_ex(spec_verify_t h, int batch, const void* target_logits, const 
   int rc = launch_fused(h, P, (long long)batch * (h->k + 1), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s);
+}
+
+int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                     int32_t* out_tokens, int32_t* out_tau, void* cuda_stream) {
+  if (!h || batch < 0 || batch > h->max_batch) return SV_ERR_ARG;
+  if (batch == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !temperature || !uniforms || !out_tokens || !out_tau)
+    return SV_ERR_ARG;
+  const int es = h->dtype == SV_FP32 ? 4 : 2;
+  if (((uintptr_t)target_logits % es) || ((uintptr_t)draft_logits % es)) return SV_ERR_ARG;
+  if (!al4(draft_tokens) || !al4(temperature) || !al4(uniforms) || !al4(out_tokens) || !al4(out_tau)) return SV_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)cuda_stream;
+  KParams P;
+  memset(&P, 0, sizeof P);
+  P.target = target_logits; P.draft = draft_logits; P.tokens = draft_tokens; P.temperature = temperature;
+  P.uniforms = uniforms;
+  P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
+  P.ws_next = h->ws_next;
+  P.flags = h->d_flags;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.units_per_chain = h->k + 1; P.tv_only = 0;
+  P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  for (int pos = 0; pos <= h->k; ++pos) {   // one launch per position, over the chains still verifying
+    P.lazy_pos = pos;
+    const int rc = launch_fused(h, P, batch, s, false, true);
+    if (rc != SV_OK) return rc;
+  }
+  return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s, true);
 }
 
 int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype, const void* target_logits,

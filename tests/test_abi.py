@@ -51,6 +51,7 @@ def test_host_side_argument_checks(lib):
     assert lib.spec_verify_init(ctypes.byref(h), 1 << 28, 7, 100, 0, 0) == 3   # B*(k+1) reaches 2^31
     assert lib.spec_verify_ex(None, 1, *([None] * 13)) == sv.SV_ERR_ARG
     assert lib.spec_verify_loss_grad(None, 1, None, None, None, 0, None, None, None, None) == sv.SV_ERR_ARG
+    assert lib.spec_verify_lazy(None, 1, *([None] * 8)) == sv.SV_ERR_ARG
     assert lib.spec_verify(None, 1, *([None] * 11)) == sv.SV_ERR_ARG
     assert lib.spec_verify_tv(None, 1, *([None] * 5)) == sv.SV_ERR_ARG
     assert lib.spec_verify_get_error(None, None) == sv.SV_ERR_ARG
