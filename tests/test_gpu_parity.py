@@ -153,6 +153,25 @@ def test_host_entry_point(lib):
     v.close()
 
 
+def test_host_entry_point_larger_batch(lib):
+    """300 chains through spec_verify_host, twice on the same staging buffers:
+    the outputs equal those of the device-pointer path."""
+    w = si.Workload("host_chunks", 300, 5, 4096, si.BF16, 2.0, draft_sigma=0.6, temp_mode=1, temp_lo=0.0, temp_hi=1.2)
+    b = si.generate(w)
+    dev, _, _ = run_gpu(lib, w, b)
+    v = lib.SpecVerifier(w.batch, w.k, w.vocab, torch.bfloat16, flags=lib.SV_FLAG_HOST_STAGING)
+    tg = torch.from_numpy(b.target.view(np.int16)).view(torch.bfloat16).pin_memory()
+    dr = torch.from_numpy(b.draft.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_out = {k: t.pin_memory() for k, t in v.alloc_outputs(w.batch, want_pq=True, want_tv=True, device="cpu").items()}
+    for _ in range(2):   # the second call reuses the staging buffers
+        v.verify_host(tg, dr, torch.from_numpy(b.tokens), torch.from_numpy(b.temperature),
+                      torch.from_numpy(b.uniforms), host_out)
+        torch.cuda.synchronize()
+        for key in dev:
+            assert np.array_equal(dev[key], host_out[key].numpy(), equal_nan=True), key
+    v.close()
+
+
 def test_empty_batch_and_bad_args(lib):
     v = lib.SpecVerifier(4, 3, 64, torch.float32)
     e = torch.empty((0, 4, 64), device="cuda")
