@@ -16,10 +16,12 @@
 //   * Pass A (registers): per-row maximum, then sum of exp2(z*c - R) with an
 //     integer reference R = ceil(max*c), c = log2(e)/T.  Integer references
 //     make every rescale between warps and CTAs an exact power of two.
-//   * Exchange (DSMEM, no cluster barrier): every warp sends its (max, sum) of
-//     both rows to every CTA with st.async, which completes the bytes on the
-//     receiver's mbarrier; each warp merges the C*8 parts in the same order,
-//     so all CTAs hold identical row statistics.
+//   * Exchange (DSMEM, no cluster barrier): every warp sends its (max, sum,
+//     integer reference) of both rows to every CTA with st.async, which
+//     completes the bytes on the receiver's mbarrier; warp 0 of each CTA
+//     merges the C*8 parts (in the same order in every CTA, so all CTAs hold
+//     identical row statistics) and hands them to the other warps through
+//     shared memory and a named barrier.
 //   * Pass B (registers): with e_j = 2^(z_j*c - R) and r = S_t/S_d, the
 //     residual weight w_j = max(0, e_t - r*e_d) = S_t * max(0, p_j - q_j) (one
 //     rounding, exactly zero for identical rows).  Each warp writes the sum of
@@ -30,6 +32,13 @@
 //     the warp range holding u * (total mass) of unit tau, re-reads that one
 //     range (1/(8C) of the rows) and finishes the inverse-CDF draw.
 //   Greedy chains (T == 0) use only the maximum and its lowest index.
+//   Units are taken position-major (u = position * B + chain).
+//
+// Variants of the same kernel (compile-time flags): ENT also sums e*a in pass
+// A and writes the entropy of every row; LAZY verifies one position per
+// launch for the chains still verifying (spec_verify_lazy).  A second kernel,
+// sv_grad_kernel, uses the same clusters, stage and exchange for the TV and
+// overlap losses and their draft-logit gradients (spec_verify_loss_grad).
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -1052,6 +1061,7 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
 // Loss: TV = 1 - alpha (SV_LOSS_TV) or -ln alpha (SV_LOSS_OVERLAP).
 
 __device__ __forceinline__ u64 mul2(u64 a, u64 b) { u64 d; asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b)); return d; }
+// Two fp32 values as one bf16x2 word (lo in the low half), rounded to nearest even.
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -1078,9 +1088,6 @@ __device__ __forceinline__ void store_grad(void* row, int v, int slen, bool vec_
     else reinterpret_cast<uint16_t*>(row)[e0 + e] = (uint16_t)((e & 1) ? (word >> 16) : (word & 0xffffu));
   }
 }
-// Two gradient values packed for the logit dtype: one bf16x2 word (rounded to
-// nearest even) for bf16, or the low value's bits (the caller pairs words) for fp32.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) { return bf16x2_rn(lo, hi); }
 
 // Sum of 32-byte exchange items l and l + 32 over the warp, for the s_t and s_d fields.
 __device__ __forceinline__ void warp_sum_items(const X1* it, int items, float& a, float& d) {
@@ -1309,7 +1316,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
       float g0, g1;
       upk(mul2(pk(ex2(ad0), ex2(ad1)), pk(s0, s1)), g0, g1);
       if constexpr (sizeof(Tl) == 4) { wd[e] = __float_as_uint(g0); wd[e + 1] = __float_as_uint(g1); }
-      else wd[e >> 1] = pack_bf16x2(g0, g1);
+      else wd[e >> 1] = bf16x2_rn(g0, g1);   // rounded to nearest even
     }
     if (j * 32 + lane < P.wv)
       store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(wd[0], wd[1], wd[2], wd[3]));
