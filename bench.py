@@ -386,8 +386,9 @@ def main(argv=None):
                                         "api": "spec_verify_ex (entropy of every target and draft row)"}
         so.close()
         del di, oo, bo
-        # lazy verification (no TV) on the workloads without TV: whole call timed with events
-        for wo in (si.C3_T1, si.C4):
+        # lazy verification (no TV): whole call timed with events; its bytes are the rows
+        # actually read, (tau + 1) row pairs per chain, or k pairs and the bonus row
+        for wo in (si.C3_T1, si.C4, w0 if w0.batch <= 1024 else w0.scaled(batch=1024)):
             bo = si.generate(wo)
             di = device_batch(bo, device)
             so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16" if wo.dtype == si.BF16 else "fp32")
@@ -404,9 +405,14 @@ def main(argv=None):
                 torch.cuda.synchronize()
                 tot += ev0.elapsed_time(ev1)
             ms = tot / 20
+            tau = np.maximum(ol["tau"].cpu().numpy().astype(np.int64), 0)
+            rows = np.where(tau < wo.k, 2 * (tau + 1), 2 * wo.k + 1)
+            lb = int(rows.sum()) * wo.vocab * (2 if wo.dtype == si.BF16 else 4)
             others[wo.name + "+lazy"] = {"call_us": 1e3 * ms, "draft_tokens_per_s": wo.batch * wo.k / (ms / 1e3),
-                                         "chains_per_s": wo.batch / (ms / 1e3), "mean_tau": float(ol["tau"].float().mean().item()),
-                                         "launches_per_call": wo.k + 2,
+                                         "chains_per_s": wo.batch / (ms / 1e3), "mean_tau": float(tau.mean()),
+                                         "bytes_read": lb, "gbps": lb / (ms / 1e3) / 1e9,
+                                         "frac_of_peak": lb / (ms / 1e3) / 1e9 / peak,
+                                         "launches_per_call": 2,
                                          "api": "spec_verify_lazy (rows past the first rejection are not read; whole call)"}
             so.close()
             del di, ol, bo

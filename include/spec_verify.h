@@ -117,8 +117,10 @@ int spec_verify(spec_verify_t h, int batch,
  * stop are valid; a chain is invalid (tau = -1) only if a row it reads is
  * (rows after the stop are never read, so their contents do not matter).
  * There is no p, q or TV output (positions after the stop are not
- * evaluated).  k + 2 kernel launches: one per position 0..k, each over the
- * chains still verifying, then the finalize kernel. */
+ * evaluated), and accepted positions skip the residual pass.  Two kernel
+ * launches: one walks every chain position by position up to its stop
+ * (each cluster of CTAs takes its share of the chains, two at a time), then
+ * the finalize kernel draws the final tokens. */
 int spec_verify_lazy(spec_verify_t h, int batch,
                      const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, const float* temperature, const float* uniforms,

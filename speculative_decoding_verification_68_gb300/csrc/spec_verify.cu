@@ -35,8 +35,8 @@
 //   Units are taken position-major (u = position * B + chain).
 //
 // Variants of the same kernel (compile-time flags): ENT also sums e*a in pass
-// A and writes the entropy of every row; LAZY verifies one position per
-// launch for the chains still verifying (spec_verify_lazy).  A second kernel,
+// A and writes the entropy of every row; LAZY walks each chain position by
+// position and stops at its first rejection (spec_verify_lazy).  A second kernel,
 // sv_grad_kernel, uses the same clusters, stage and exchange for the TV and
 // overlap losses and their draft-logit gradients (spec_verify_loss_grad).
 #include <cuda_runtime.h>
@@ -105,11 +105,7 @@ struct KParams {
   void* grad;                // [B, k, V] in the logit dtype
   int loss_kind;             // SV_LOSS_TV or SV_LOSS_OVERLAP
   int grad_vec;              // gradient rows can take 16-byte stores
-  // lazy verification (one launch per position)
-  int lazy_pos;              // the position this launch verifies
-  int* ws_next;              // [B] the next position a chain waits for (LAZY_DONE: stopped)
 };
-constexpr int LAZY_DONE = 0x7fffffff;
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
   float m_t, m_d;              // maxima of the warp's range in the target / draft row
@@ -126,7 +122,7 @@ struct alignas(16) Merged {
   float r;             // S_t / S_d
   int IR_t;            // R_t as an integer (NO_REF if the row has no finite maximum)
   int status;          // ST_* bits, 0 if valid
-  int pad;
+  int cont;            // lazy verification: the chain goes on to the next position
 };
 
 struct Small {
@@ -509,8 +505,10 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
 __device__ __forceinline__ void merged_arrive() { asm volatile("bar.arrive 1, %0;" ::"n"(NT) : "memory"); }
 __device__ __forceinline__ void merged_wait() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
+// Returns, for lazy verification, whether the chain goes on to its next
+// position (the same in every CTA of the cluster); 0 otherwise.
 template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
-__device__ __forceinline__ void process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
+__device__ __forceinline__ int process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
                                              const float T, const int x) {
@@ -519,6 +517,15 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, V = P.V;
   const int b = un.b, ipos = un.ipos;
+
+  // Lazy verification takes the accept decision in every CTA at the merge:
+  // the logits at the drafted token and the uniform are loaded ahead of it.
+  float lz_t = 0.0f, lz_d = 0.0f, lz_u = 0.0f;
+  if (LAZY && PAIR && tid == 0 && x >= 0 && x < V) {
+    lz_t = Lay<Tl>::load_scalar(P.target, ((long long)b * (k + 1) + ipos) * V + x);
+    lz_d = Lay<Tl>::load_scalar(P.draft, ((long long)b * k + ipos) * V + x);
+    lz_u = P.uniforms[(size_t)b * (k + 1) + ipos];
+  }
 
   // ---------------- this warp's vectors of the unit into registers
   uint4 rt[R], rd[R];
@@ -530,7 +537,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       rt[j] = blk_t[j * 32 + lane];
       if (PAIR) rd[j] = blk_d[j * 32 + lane];
     }
-    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
+    own_x = !LAZY && PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
       const int lx = (int)(x - g.slice0());
       const int lv = lx / EPV, wb = lv / P.wv, iv = lv - wb * P.wv;
@@ -554,7 +561,7 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       rt[j] = load_vec_direct<Tl>(tb, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
       if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
     }
-    own_x = PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
+    own_x = !LAZY && PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
       S.gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
       S.gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
@@ -708,8 +715,17 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
       }
     }
     if (lane == 0) {
+      int cont = 0;   // the same test as the accept test below, on the same values
+      if (LAZY && PAIR && status == 0) {
+        if (greedy) {
+          cont = x == A_t;
+        } else {
+          const float lpx = fmaf(lz_t, c, -R_t), lqx = fmaf(lz_d, c, -R_d);
+          cont = lz_u < exp2f(lpx - lqx) * (S_d / S_t);
+        }
+      }
       Merged m;
-      m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.pad = 0;
+      m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
       mg = m;
       if (g.rank() == 0) {
         UnitStat st;
@@ -723,14 +739,12 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
               P.ws_acc[pi] = x == A_t;
               if (P.out_p) P.out_p[pi] = x == A_t ? 1.0f : 0.0f;
               if (P.out_q) P.out_q[pi] = x == A_d ? 1.0f : 0.0f;
-              if (LAZY) P.ws_next[b] = x == A_t ? ipos + 1 : LAZY_DONE;
             }
           }
-          if (LAZY && PAIR && status != 0) {   // an invalid position stops the chain
-            P.ws_acc[pi] = 0;
-            P.ws_next[b] = LAZY_DONE;
-          }
+          if (LAZY && PAIR && status != 0) P.ws_acc[pi] = 0;   // an invalid position stops the chain
           if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
+        } else if (LAZY && PAIR) {
+          P.ws_acc[pi] = cont;
         }
       }
     }
@@ -740,14 +754,15 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
     merged_wait();
   }
   const Merged M = mg;
-  if (M.status != 0 || greedy) return;   // cluster-uniform
+  // cluster-uniform; an accepted position of a lazy walk needs no residual
+  if (M.status != 0 || greedy || (LAZY && M.cont)) return M.cont;
 
   // this range's part of S_t (the target mass, and the draw from p when the residual is zero)
   const float pmass = mine.s_t * pow2_diff(mine.ref_t, M.IR_t);
   const size_t item = ui * ITEMS_MAX + g.rank() * NWARP + warp;
   if (!PAIR) {   // the bonus row: its mass is already known
     if (lane == 0) { P.ws_p[item] = pmass; P.ws_w[item] = pmass; }
-    return;
+    return 0;
   }
   if (lane == 0) P.ws_p[item] = pmass;
 
@@ -763,15 +778,15 @@ __device__ __forceinline__ void process_unit(const KParams& P, Small& S, const u
   }
   const float wwarp = warp_sum_f32(w0 + w1);
   if (lane == 0) P.ws_w[item] = wwarp;
-  if (own_x && tid == 0) {   // accept test at the drafted token
+  if (!LAZY && own_x && tid == 0) {   // accept test at the drafted token
     const float lpx = fmaf(S.gz_t, c, -M.R_t), lqx = fmaf(S.gz_d, c, -M.R_d);
     const float ratio = exp2f(lpx - lqx) * (M.S_d / M.S_t);
     const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
     P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
-    if (LAZY) P.ws_next[b] = u_acc < ratio ? ipos + 1 : LAZY_DONE;
     if (P.out_p) P.out_p[pi] = exp2f(lpx) / M.S_t;
     if (P.out_q) P.out_q[pi] = exp2f(lqx) / M.S_d;
   }
+  return 0;
 }
 
 template <typename Tl, int R, bool ENT, bool LAZY>
@@ -809,32 +824,42 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
   if constexpr (LAZY) {
-    // One position for every chain still verifying at it: the chains this
-    // cluster owns (b = cluster_id mod n_clusters) whose next position is
-    // P.lazy_pos.  A chain's flag is written only after the cluster has
-    // exchanged that chain's statistics, by which time every CTA of the
-    // cluster has read it, so all CTAs walk the same chains.
-    const int pos = P.lazy_pos;
-    auto waiting = [&](unsigned bb) { return pos == 0 || __ldcg(&P.ws_next[bb]) == pos; };
-    unsigned u = cid;
-    while (u < B && !waiting(u)) u += ncl;
-    Unit cur;
-    cur.b = (int)u; cur.ipos = pos;
-    if (P.tma && warp == 0 && u < B) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
-    while (u < B) {
-      unsigned un = u + ncl;
-      while (un < B && !waiting(un)) un += ncl;
-      Unit next;
-      next.b = (int)un; next.ipos = pos;
+    // Each cluster walks its chains b = cluster_id, cluster_id + n_clusters,
+    // ... position by position and stops a chain at its first rejection (or
+    // after its bonus row).  Two chains are in flight, taking turns, so that
+    // the unit after the current one is always known (the other chain's next
+    // position, decided one unit earlier) and its copy can be issued ahead.
+    // The walk is the same in every CTA of the cluster: it depends only on
+    // the accept decisions, which every CTA takes from the merged statistics.
+    unsigned jn = 0;   // the next chain of this cluster's list to start
+    auto take = [&]() {
+      Unit t;
+      t.ipos = 0;
+      t.b = -1;
+      if (cid + (unsigned long long)jn * ncl < B) { t.b = (int)(cid + jn * ncl); ++jn; }
+      return t;
+    };
+    Unit cur = take(), nxt = take();
+    bool loaded = false;   // cur's copy was issued while the previous unit ran
+    while (cur.b >= 0) {
+      if (P.tma && !loaded) {   // nothing issued ahead: every warp is done with the stage
+        __syncthreads();
+        if (warp == 0) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+      }
+      const bool has_next = nxt.b >= 0;
       const float T = P.temperature[cur.b];
-      const int x = pos < k ? P.tokens[(size_t)cur.b * k + pos] : 0;
-      if (pos < k)
-        process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && un < B, T, x);
+      const int x = cur.ipos < k ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
+      int cont;
+      if (cur.ipos < k)
+        cont = process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt, P.tma && has_next, T, x);
       else
-        process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && un < B, T, x);
-      cur = next;
-      u = un;
+        cont = process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt, P.tma && has_next, T, x);
       phase ^= 1u;
+      Unit after;
+      if (cont) { after.b = cur.b; after.ipos = cur.ipos + 1; }
+      else after = take();
+      if (has_next) { cur = nxt; nxt = after; loaded = true; }
+      else { cur = after; loaded = false; }
     }
   } else {
     unsigned u = cid;
@@ -1212,7 +1237,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
         Merged m;
         m.S_t = S_t; m.S_d = S_d;
         m.R_t = IR_t == NO_REF ? 0.0f : (float)IR_t; m.R_d = IR_d == NO_REF ? 0.0f : (float)IR_d;
-        m.r = row_ok ? S_t / S_d : 0.0f; m.IR_t = IR_t; m.status = row_ok ? 0 : ST_ROW; m.pad = 0;
+        m.r = row_ok ? S_t / S_d : 0.0f; m.IR_t = IR_t; m.status = row_ok ? 0 : ST_ROW; m.cont = 0;
         mg = m;
       }
       __syncwarp();
@@ -1421,9 +1446,8 @@ struct spec_verify_ctx {
   int n_clusters_ent;
   FusedFn kernel_grad;       // loss-gradient kernel
   int n_clusters_grad;
-  FusedFn kernel_lazy;       // one position of lazy verification
+  FusedFn kernel_lazy;       // lazy verification (each chain up to its first rejection)
   int n_clusters_lazy;
-  int* ws_next;              // [max_batch] next position of each chain (lazy)
   FinalFn finalize;
   int32_t* ws_acc;
   int32_t* ws_y;
@@ -1451,7 +1475,7 @@ static constexpr int TIMING_RING = 4096;
 
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
-  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->ws_next, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
+  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
                   h->st_unif, h->st_out_tokens, h->st_out_tau, h->st_out_p, h->st_out_q, h->st_out_tv};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -1709,8 +1733,7 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
             cudaMalloc(&h->ws_stat, mb * (k + 1) * sizeof(UnitStat)) == cudaSuccess &&
             cudaMalloc(&h->ws_w, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->ws_p, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess &&
-            cudaMalloc(&h->ws_next, mb * sizeof(int)) == cudaSuccess;
+            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess;
   if (ok && (flags & SV_FLAG_HOST_STAGING)) {
     const size_t rowb = (size_t)vocab * es;
     ok = cudaMalloc(&h->st_target, mb * (k + 1) * rowb) == cudaSuccess &&
@@ -1800,16 +1823,12 @@ int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, cons
   P.target = target_logits; P.draft = draft_logits; P.tokens = draft_tokens; P.temperature = temperature;
   P.uniforms = uniforms;
   P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
-  P.ws_next = h->ws_next;
   P.flags = h->d_flags;
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
-  for (int pos = 0; pos <= h->k; ++pos) {   // one launch per position, over the chains still verifying
-    P.lazy_pos = pos;
-    const int rc = launch_fused(h, P, batch, s, false, true);
-    if (rc != SV_OK) return rc;
-  }
+  const int rc = launch_fused(h, P, batch, s, false, true);
+  if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s, true);
 }
 

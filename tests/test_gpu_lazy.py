@@ -82,3 +82,33 @@ def test_lazy_reads_only_up_to_the_stop(lib):
     assert lazy2["tau"][c1] == tau[c1] and np.array_equal(lazy2["tokens"][c1], lazy["tokens"][c1])
     assert full2["tau"][c1] == -1
     assert lazy2["tau"][c2] == -1 and full2["tau"][c2] == -1
+
+
+def test_lazy_all_accepted_walks_to_the_bonus(lib, oracle):
+    """Identical draft and target rows accept every draft: every chain walks
+    all k positions and draws its bonus token from target row k."""
+    w = si.Workload("lazy_same", 50, 5, 4099, si.BF16, 2.0, draft_sigma=0.0)
+    b = si.generate(w)
+    assert np.array_equal(b.draft, b.target[:, :w.k])
+    full, lazy, lazy2 = run(lib, w, b)
+    assert np.all(lazy["tau"] == w.k)
+    for key in ("tokens", "tau"):
+        assert np.array_equal(full[key], lazy[key]) and np.array_equal(lazy[key], lazy2[key]), key
+    ref = oracle.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, want_tv=False, nthreads=16)
+    _parity.token_parity(lazy, ref, w.k)
+
+
+@pytest.mark.parametrize("B", [1, 2, 5, 37, 73])
+def test_lazy_chain_counts(lib, oracle, B):
+    """Fewer chains than clusters, one or two per cluster, and more: each
+    cluster walks its share of the chains two at a time."""
+    w = si.Workload(f"lazy_b{B}", B, 3, 151552, si.BF16, 2.0, draft_sigma=0.6, temp_mode=1, temp_lo=0.5,
+                    temp_hi=1.2)
+    b = si.generate(w)
+    full, lazy, lazy2 = run(lib, w, b)
+    for key in ("tokens", "tau"):
+        assert np.array_equal(full[key], lazy[key]) and np.array_equal(lazy[key], lazy2[key]), key
+    ref = oracle.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, want_tv=False, nthreads=16)
+    _parity.token_parity(lazy, ref, w.k)
+    if B >= 2:   # with these seeds chain 1 accepts all three drafts
+        assert lazy["tau"].max() == w.k
