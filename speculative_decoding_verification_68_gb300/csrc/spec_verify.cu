@@ -912,24 +912,40 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   const int k = F.k, items = F.items;
   const size_t ub = (size_t)b * (k + 1);
   const int npos = F.tv_only ? k : k + 1;
-  int last = npos - 1;   // the last position whose unit was verified
-  if (F.lazy) {          // only positions up to the first rejection were: find it first
-    const int a0 = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
-    const unsigned rej0 = __ballot_sync(FULL, lane < k && a0 == 0);
-    last = rej0 ? __ffs(rej0) - 1 : k;
-  }
+  // accept bits (not written, and not used, for TV only)
+  const int a = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
+  const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
+  const int tau = rej ? __ffs(rej) - 1 : k;
+  // the last position whose unit was verified: a lazy walk stopped at the first rejection
+  const int last = F.lazy ? tau : npos - 1;
   const int st = lane < npos && lane <= last ? F.ws_stat[ub + lane].status : 0;
   const bool bad = __any_sync(FULL, st != 0);
 
-  // TV of every valid, non-greedy position
+  // TV of every valid, non-greedy position: 8 positions per pass, 4 lanes per
+  // position, each lane adding 16 consecutive range masses (loaded together)
   if (F.out_tv) {
-    for (int i = 0; i < k; ++i) {
-      const UnitStat us = F.ws_stat[ub + i];
-      if (us.status != 0 || us.greedy) continue;
-      const float* w = F.ws_w + (ub + i) * ITEMS_MAX;
-      float v = (lane < items ? w[lane] : 0.0f) + (lane + 32 < items ? w[lane + 32] : 0.0f);
-      v = warp_sum_f32(v);
-      if (lane == 0) F.out_tv[(size_t)b * k + i] = v / us.S_t;
+    for (int i0 = 0; i0 < k; i0 += 8) {
+      const int i = i0 + (lane >> 2), q = lane & 3;
+      float v = 0.0f, S_t = 1.0f;
+      bool ok = false;
+      if (i < k) {
+        const UnitStat us = F.ws_stat[ub + i];
+        ok = us.status == 0 && !us.greedy;
+        S_t = us.S_t;
+        const float4* w4 = reinterpret_cast<const float4*>(F.ws_w + (ub + i) * ITEMS_MAX) + q * 4;
+        float4 w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = w4[e];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int it = q * 16 + e * 4;   // ranges past `items` were never written
+          v += (it < items ? w[e].x : 0.0f) + (it + 1 < items ? w[e].y : 0.0f) +
+               (it + 2 < items ? w[e].z : 0.0f) + (it + 3 < items ? w[e].w : 0.0f);
+        }
+      }
+      v += __shfl_xor_sync(FULL, v, 1);
+      v += __shfl_xor_sync(FULL, v, 2);
+      if (q == 0 && ok) F.out_tv[(size_t)b * k + i] = v / S_t;
     }
   }
   if (bad && lane == 0) atomicAdd(&F.flags[0], 1);
@@ -939,9 +955,6 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
     if (lane == 0) F.out_tau[b] = -1;
     return;
   }
-  const int a = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
-  const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
-  const int tau = rej ? __ffs(rej) - 1 : k;
   const bool pair = tau < k;
   const size_t uu = ub + tau;
   const UnitStat us = F.ws_stat[uu];
