@@ -213,6 +213,12 @@ def measure_kernel(sv, dev_inputs, out, steps, flush=None):
     return statistics.mean(kt), kt
 
 
+def spread_us(kt):
+    """p10 / p50 / p90 of kernel durations given in ms, in microseconds."""
+    q = np.percentile(np.asarray(kt, dtype=np.float64) * 1e3, [10, 50, 90])
+    return {"p10": float(q[0]), "p50": float(q[1]), "p90": float(q[2]), "n": len(kt)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -362,9 +368,12 @@ def main(argv=None):
             oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device)
             for _ in range(3):
                 so.verify(*di, out=oo)
-            kms, _ = measure_kernel(so, di, oo, 20, flush=flush)
+            kms, kto = measure_kernel(so, di, oo, 20, flush=flush)
+            kms_warm, _ = measure_kernel(so, di, oo, 20)   # no flush: inputs below L2 size stay resident
             ob = wo.logit_bytes
-            others[wo.name] = {"kernel_us": 1e3 * kms, "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
+            others[wo.name] = {"kernel_us": 1e3 * kms, "kernel_us_spread": spread_us(kto),
+                               "kernel_us_warm": 1e3 * kms_warm,
+                               "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
                                "chains_per_s": wo.batch / (kms / 1e3), "gbps": ob / (kms / 1e3) / 1e9,
                                "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
                                "mean_tau": float(oo["tau"].float().mean().item())}
@@ -384,8 +393,23 @@ def main(argv=None):
         others[wo.name + "+entropy"] = {"kernel_us": 1e3 * kms, "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
                                         "gbps": ob / (kms / 1e3) / 1e9, "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
                                         "api": "spec_verify_ex (entropy of every target and draft row)"}
+        # ... and through spec_verify_tv: the TV of every position only (no accept tests, no bonus rows)
+        otv = torch.empty((wo.batch, wo.k), dtype=torch.float32, device=device)
+        for _ in range(3):
+            so.verify_tv(di[0], di[1], di[3], out=otv)
+        so.kernel_times()
+        for _ in range(20):
+            flush.zero_()
+            so.verify_tv(di[0], di[1], di[3], out=otv)
+        torch.cuda.synchronize()
+        kms = statistics.mean(so.kernel_times())
+        tb = wo.batch * 2 * wo.k * wo.vocab * (2 if wo.dtype == si.BF16 else 4)
+        others[wo.name + "+tv_only"] = {"kernel_us": 1e3 * kms, "positions_per_s": wo.batch * wo.k / (kms / 1e3),
+                                        "bytes": tb, "gbps": tb / (kms / 1e3) / 1e9,
+                                        "frac_of_peak": tb / (kms / 1e3) / 1e9 / peak,
+                                        "api": "spec_verify_tv (TV of every position only)"}
         so.close()
-        del di, oo, bo
+        del di, oo, bo, otv
         # lazy verification (no TV): whole call timed with events; its bytes are the rows
         # actually read, (tau + 1) row pairs per chain, or k pairs and the bonus row
         for wo in (si.C3_T1, si.C4, w0 if w0.batch <= 1024 else w0.scaled(batch=1024)):
@@ -463,6 +487,7 @@ def main(argv=None):
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic["dram_bytes_per_launch"] * nb / traffic["batch"] if traffic else None,
                          "kernel": "sv_fused_kernel", "kernel_ms": kernel_ms,
+                         "kernel_us_spread": spread_us(kt) if kt else None,
                          "algorithmic_bytes_per_launch": alg_bytes},
             "gpu_launches": args.steps * info["launches_per_call"],
             "clocks": clocks,
