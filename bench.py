@@ -352,7 +352,8 @@ def main(argv=None):
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
         e2e = {"value": chains_total * w.k / (e2e_ms / args.steps / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.steps, "api": "spec_verify_host (pinned host buffers)"}
+               "ms_per_step": e2e_ms / args.steps,
+               "api": "spec_verify_host (pinned host buffers: logits read in place over the host link)"}
         sv_h.close()
         del host_in, host_out
 

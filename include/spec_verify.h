@@ -210,12 +210,15 @@ int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype,
 int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
                    const float* temperature, float* out_tv, void* cuda_stream);
 
-/* spec_verify for callers whose inputs and outputs live in host memory
- * (pinned memory gives the fastest copies).  Same arguments and layouts as
- * spec_verify, but every pointer is a host pointer; the handle must have been
- * created with SV_FLAG_HOST_STAGING.  Copies inputs to the handle's device
- * staging, verifies, copies outputs back, all on `cuda_stream`; the call
- * returns after enqueueing (synchronise the stream before reading outputs). */
+/* spec_verify for callers whose inputs and outputs live in host memory.
+ * Same arguments and layouts as spec_verify, but every pointer is a host
+ * pointer; the handle must have been created with SV_FLAG_HOST_STAGING.
+ * Logits in page-locked memory that the device can address (pinned memory on
+ * a system with unified addressing) are read in place by the kernels over the
+ * host link; other logits are first copied into the handle's device staging.
+ * The small inputs go through the staging, and the outputs are copied back,
+ * all on `cuda_stream`.  The call returns after enqueueing (synchronise the
+ * stream before reading outputs); the host buffers must stay valid until then. */
 int spec_verify_host(spec_verify_t h, int batch,
                      const void* host_target_logits, const void* host_draft_logits,
                      const int32_t* host_draft_tokens, const float* host_temperature,
@@ -229,6 +232,17 @@ int spec_verify_host(spec_verify_t h, int batch,
  * *invalid_count if non-NULL), SV_ERR_TIMEOUT, or SV_ERR_CUDA.  Clears the
  * flags. */
 int spec_verify_get_error(spec_verify_t h, int* invalid_count);
+
+/* Self-test of the bounded device waits (for tests).  One thread waits on a
+ * shared-memory barrier that nothing completes, first with the kernels' stage
+ * wait and then with their cluster-scope wait, each limited to `polls` polls
+ * (the kernels use 2^18, about one second).  The first wait must give up and set the handle's
+ * timeout flag; the second must then see the flag and return early.  Nothing
+ * is left in flight, so the context stays usable.  Synchronises, stores the
+ * SM clock cycles each wait took in elapsed_cycles[0..1] (nullable), and
+ * returns what spec_verify_get_error returns: SV_ERR_TIMEOUT when the waits
+ * expired as they should.  SV_ERR_ARG for polls < 1. */
+int spec_verify_selftest_wait(spec_verify_t h, int polls, long long* elapsed_cycles);
 
 /* Launch geometry chosen at init: vocabulary slices per row (thread-block
  * cluster size), persistent clusters, register rounds per thread, whether

@@ -182,8 +182,10 @@ class SpecVerifier:
         return out
 
     def verify_host(self, target, draft, tokens, temperature, uniforms, out: dict, stream=None) -> dict:
-        """spec_verify_host: host (preferably pinned) tensors in and out; the
-        handle needs SV_FLAG_HOST_STAGING.  Synchronise the stream before reading out."""
+        """spec_verify_host: host tensors in and out; the handle needs
+        SV_FLAG_HOST_STAGING.  Pinned logits are read in place by the kernels,
+        pageable ones copied to the device first.  Synchronise the stream
+        before reading out."""
         B = self._check_inputs(target, draft, tokens, temperature, uniforms)
         rc = self._lib.spec_verify_host(self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature),
                                         _ptr(uniforms), _ptr(out["tokens"]), _ptr(out["tau"]),
@@ -199,6 +201,12 @@ class SpecVerifier:
         n = ctypes.c_int(0)
         _check(self._lib.spec_verify_kernel_times(self._h, buf, max_n, ctypes.byref(n)), "spec_verify_kernel_times")
         return list(buf[:n.value])
+
+    def selftest_wait(self, polls: int):
+        """spec_verify_selftest_wait: (status, [cycles of the first wait, of the second])."""
+        c = (ctypes.c_longlong * 2)()
+        rc = self._lib.spec_verify_selftest_wait(self._h, int(polls), c)
+        return rc, [c[0], c[1]]
 
     def get_error(self):
         """Synchronise; return (status, invalid_count) and clear the device flags."""

@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_host.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_get_error.restype = i
     lib.spec_verify_get_error.argtypes = [vp, p(i)]
+    lib.spec_verify_selftest_wait.restype = i
+    lib.spec_verify_selftest_wait.argtypes = [vp, i, p(ctypes.c_longlong)]
     lib.spec_verify_info.restype = i
     lib.spec_verify_info.argtypes = [vp, p(i), p(i), p(i), p(i), p(i)]
     lib.spec_verify_kernel_times.restype = i

@@ -98,7 +98,8 @@ struct KParams {
   int wv;                    // vectors per warp: ceil(ceil(Vs / EPV) / NWARP)
   int units_per_chain;       // k+1 (verify) or k (TV only)
   int tv_only;
-  int tma;
+  int tma;                   // bulk copies into the stage
+  int vec16;                 // without them: rows 16-byte aligned, so 16-byte loads
   // loss-gradient kernel
   const float* weights;      // [B, k] or null (all 1)
   float* out_loss;           // [B, k] or null
@@ -172,16 +173,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, unsigned parity) {
   return ok != 0;
 }
 // Bounded wait for a stage: gives up (and flags the handle) instead of hanging.
-__device__ __forceinline__ void mbar_wait_bounded(uint32_t a, unsigned parity, int* flags) {
-  for (int it = 0; it < (1 << 22); ++it) {
+// Once any wait has given up, the others see the flag and return within 256 polls.
+constexpr int WAIT_POLLS = 1 << 18;   // about 1 s: a poll suspends for ~3.8 us on GB300
+__device__ __forceinline__ void mbar_wait_bounded(uint32_t a, unsigned parity, int* flags, int polls = WAIT_POLLS) {
+  for (int it = 0; it < polls; ++it) {
     if (mbar_try(a, parity)) return;
     if ((it & 255) == 255 && *(volatile int*)&flags[1]) return;
   }
   atomicExch(&flags[1], 1);
 }
 // Bounded wait for data that peers of the cluster deliver (acquire at cluster scope).
-__device__ __forceinline__ void mbar_wait_cluster_bounded(uint32_t a, unsigned parity, int* flags) {
-  for (int it = 0; it < (1 << 22); ++it) {
+__device__ __forceinline__ void mbar_wait_cluster_bounded(uint32_t a, unsigned parity, int* flags,
+                                                          int polls = WAIT_POLLS) {
+  for (int it = 0; it < polls; ++it) {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok) : "r"(a), "r"(parity) : "memory");
@@ -558,8 +562,14 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const int v = g.vbeg() + j * 32 + lane;
-      rt[j] = load_vec_direct<Tl>(tb, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
-      if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen(), v < min(g.vbeg() + P.wv, nvec_of<Tl>(g)));
+      const bool in = v < min(g.vbeg() + P.wv, nvec_of<Tl>(g));
+      if (P.vec16) {   // the tail vector of a 16-byte-aligned row is whole (the row length is too)
+        rt[j] = in ? __ldg(reinterpret_cast<const uint4*>(tb) + v) : Lay<Tl>::neg_inf();
+        if (PAIR) rd[j] = in ? __ldg(reinterpret_cast<const uint4*>(db) + v) : Lay<Tl>::neg_inf();
+      } else {
+        rt[j] = load_vec_direct<Tl>(tb, v, g.slen(), in);
+        if (PAIR) rd[j] = load_vec_direct<Tl>(db, v, g.slen(), in);
+      }
     }
     own_x = !LAZY && PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
@@ -881,6 +891,28 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
 }
 
+// Self-test of the bounded waits: thread 0 waits on an mbarrier that nothing
+// completes, with the stage wait and then with the cluster-scope wait; both
+// must give up.  No copy or remote store is in flight, so nothing is left
+// pending when the CTA exits.
+__global__ void sv_wait_selftest_kernel(int* flags, int polls, long long* cycles) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(saddr(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    mbar_wait_bounded(saddr(&bar), 0u, flags, polls);
+    const long long t1 = clock64();
+    mbar_wait_cluster_bounded(saddr(&bar), 0u, flags, polls);   // the flag is set: returns early
+    const long long t2 = clock64();
+    cycles[0] = t1 - t0;
+    cycles[1] = t2 - t1;
+  }
+}
+
 // ------------------------------------------------------------ finalize kernel
 struct FParams {
   const void* target;
@@ -896,7 +928,7 @@ struct FParams {
   int32_t* out_tau;
   float* out_tv;
   int* flags;
-  int B, k, V, Vs, wv, items, tma, tv_only;
+  int B, k, V, Vs, wv, items, vec16, tv_only;   // vec16: rows 16-byte aligned
   int lazy;   // positions after the first rejection were not verified
 };
 
@@ -1015,7 +1047,7 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const int v = vbeg + j * 32 + lane;
-      if (F.tma) {
+      if (F.vec16) {
         rt[j] = v < vend ? __ldg(reinterpret_cast<const uint4*>(tb) + v) : Lay<Tl>::neg_inf();
         rd[j] = (use_pair && v < vend) ? __ldg(reinterpret_cast<const uint4*>(db) + v) : Lay<Tl>::neg_inf();
       } else {
@@ -1538,7 +1570,7 @@ static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* 
   F.target = P.target; F.draft = P.draft; F.tokens = tokens; F.uniforms = P.uniforms;
   F.ws_acc = P.ws_acc; F.ws_y = P.ws_y; F.ws_stat = P.ws_stat; F.ws_w = P.ws_w; F.ws_p = P.ws_p;
   F.out_tokens = out_tokens; F.out_tau = out_tau; F.out_tv = P.out_tv; F.flags = P.flags;
-  F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.wv = P.wv; F.items = h->C * NWARP; F.tma = P.tma;
+  F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.wv = P.wv; F.items = h->C * NWARP; F.vec16 = P.tma || P.vec16;
   F.tv_only = P.tv_only;
   F.lazy = lazy ? 1 : 0;
   h->finalize<<<(P.B + 7) / 8, 256, 0, s>>>(F);
@@ -1790,10 +1822,12 @@ int spec_verify(spec_verify_t h, int batch, const void* target_logits, const voi
                         out_p_draft, out_q_draft, out_tv, nullptr, nullptr, cuda_stream);
 }
 
-int spec_verify_ex(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
-                   const int32_t* draft_tokens, const float* temperature, const float* uniforms,
-                   int32_t* out_tokens, int32_t* out_tau, float* out_p_draft, float* out_q_draft, float* out_tv,
-                   float* out_entropy_target, float* out_entropy_draft, void* cuda_stream) {
+// The verification step.  bulk_ok = false keeps the kernels off bulk copies
+// (logits in host memory, read in place).
+static int verify_impl(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                       int32_t* out_tokens, int32_t* out_tau, float* out_p_draft, float* out_q_draft, float* out_tv,
+                       float* out_entropy_target, float* out_entropy_draft, void* cuda_stream, bool bulk_ok) {
   if (!h || batch < 0 || batch > h->max_batch) return SV_ERR_ARG;
   if (batch == 0) return SV_OK;
   if (!target_logits || !draft_logits || !draft_tokens || !temperature || !uniforms || !out_tokens || !out_tau)
@@ -1814,10 +1848,19 @@ int spec_verify_ex(spec_verify_t h, int batch, const void* target_logits, const 
   P.flags = h->d_flags;
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
-  P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.vec16 = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.tma = bulk_ok && P.vec16;
   int rc = launch_fused(h, P, (long long)batch * (h->k + 1), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s);
+}
+
+int spec_verify_ex(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
+                   const int32_t* draft_tokens, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_tau, float* out_p_draft, float* out_q_draft, float* out_tv,
+                   float* out_entropy_target, float* out_entropy_draft, void* cuda_stream) {
+  return verify_impl(h, batch, target_logits, draft_logits, draft_tokens, temperature, uniforms, out_tokens, out_tau,
+                     out_p_draft, out_q_draft, out_tv, out_entropy_target, out_entropy_draft, cuda_stream, true);
 }
 
 int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, const void* draft_logits,
@@ -1840,6 +1883,7 @@ int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, cons
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.vec16 = P.tma;
   const int rc = launch_fused(h, P, batch, s, false, true);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s, true);
@@ -1896,6 +1940,7 @@ int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype, const void
   P.B = batch; P.k = k; P.V = vocab; P.Vs = h.Vs; P.wv = h.wv;
   P.units_per_chain = k + 1; P.tv_only = 0;
   P.tma = h.tma_ok && al16(target_logits) && al16(draft_logits);
+  P.vec16 = P.tma;
   int rc = launch_fused(&h, P, (long long)batch * (k + 1), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(&h, P, draft_tokens, out_tokens, out_tau, s);
@@ -1917,6 +1962,7 @@ int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const 
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k; P.tv_only = 1;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.vec16 = P.tma;
   cudaStream_t s = (cudaStream_t)cuda_stream;
   int rc = launch_fused(h, P, (long long)batch * h->k, s);
   if (rc != SV_OK) return rc;
@@ -1941,8 +1987,20 @@ int spec_verify_loss_grad(spec_verify_t h, int batch, const void* target_logits,
   P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
   P.units_per_chain = h->k; P.tv_only = 1;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
+  P.vec16 = P.tma;
   P.grad_vec = ((size_t)h->V * es) % 16 == 0 && al16(grad_draft);
   return launch_fused(h, P, (long long)batch * h->k, (cudaStream_t)cuda_stream, true);
+}
+
+// The device address of host memory the device can read directly (page-locked
+// memory on a system with unified addressing), else null.
+static const void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 int spec_verify_host(spec_verify_t h, int batch, const void* host_target_logits, const void* host_draft_logits,
@@ -1958,15 +2016,25 @@ int spec_verify_host(spec_verify_t h, int batch, const void* host_target_logits,
   const int es = h->dtype == SV_FP32 ? 4 : 2;
   const size_t B = (size_t)batch, k = (size_t)h->k, rowb = (size_t)h->V * es;
   const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
-  if (cudaMemcpyAsync(h->st_target, host_target_logits, B * (k + 1) * rowb, H2D, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->st_draft, host_draft_logits, B * k * rowb, H2D, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->st_tokens, host_draft_tokens, B * k * 4, H2D, s) != cudaSuccess ||
+  // Logits in page-locked host memory that the device addresses directly are
+  // read in place by the kernels, over the host link, with 16-byte loads (no
+  // bulk copies from host memory).  Other host memory is copied into the
+  // device staging buffers first.  Either way every logit crosses the link
+  // once; reading in place saves the separate copy before the kernels.
+  const void* dev_t = device_view(host_target_logits);
+  const void* dev_d = device_view(host_draft_logits);
+  const bool in_place = dev_t && dev_d;
+  if (!in_place && (cudaMemcpyAsync(h->st_target, host_target_logits, B * (k + 1) * rowb, H2D, s) != cudaSuccess ||
+                    cudaMemcpyAsync(h->st_draft, host_draft_logits, B * k * rowb, H2D, s) != cudaSuccess))
+    return SV_ERR_CUDA;
+  if (cudaMemcpyAsync(h->st_tokens, host_draft_tokens, B * k * 4, H2D, s) != cudaSuccess ||
       cudaMemcpyAsync(h->st_temp, host_temperature, B * 4, H2D, s) != cudaSuccess ||
       cudaMemcpyAsync(h->st_unif, host_uniforms, B * (k + 1) * 4, H2D, s) != cudaSuccess)
     return SV_ERR_CUDA;
-  int rc = spec_verify(h, batch, h->st_target, h->st_draft, h->st_tokens, h->st_temp, h->st_unif, h->st_out_tokens,
-                       h->st_out_tau, host_out_p_draft ? h->st_out_p : nullptr, host_out_q_draft ? h->st_out_q : nullptr,
-                       host_out_tv ? h->st_out_tv : nullptr, cuda_stream);
+  int rc = verify_impl(h, batch, in_place ? dev_t : h->st_target, in_place ? dev_d : h->st_draft, h->st_tokens,
+                       h->st_temp, h->st_unif, h->st_out_tokens, h->st_out_tau,
+                       host_out_p_draft ? h->st_out_p : nullptr, host_out_q_draft ? h->st_out_q : nullptr,
+                       host_out_tv ? h->st_out_tv : nullptr, nullptr, nullptr, cuda_stream, !in_place);
   if (rc != SV_OK) return rc;
   if (cudaMemcpyAsync(host_out_tokens, h->st_out_tokens, B * (k + 1) * 4, D2H, s) != cudaSuccess ||
       cudaMemcpyAsync(host_out_tau, h->st_out_tau, B * 4, D2H, s) != cudaSuccess)
@@ -1988,6 +2056,23 @@ int spec_verify_get_error(spec_verify_t h, int* invalid_count) {
   if (f[1]) return SV_ERR_TIMEOUT;
   if (f[0]) return SV_ERR_DATA;
   return SV_OK;
+}
+
+int spec_verify_selftest_wait(spec_verify_t h, int polls, long long* elapsed_cycles) {
+  if (!h || polls < 1) return SV_ERR_ARG;
+  long long* d = nullptr;
+  if (cudaMalloc(&d, 2 * sizeof(long long)) != cudaSuccess) return SV_ERR_ALLOC;
+  sv_wait_selftest_kernel<<<1, 32>>>(h->d_flags, polls, d);
+  long long c[2] = {0, 0};
+  int rc = cudaGetLastError() == cudaSuccess && cudaMemcpy(c, d, sizeof c, cudaMemcpyDeviceToHost) == cudaSuccess
+               ? SV_OK : SV_ERR_CUDA;
+  cudaFree(d);
+  if (rc != SV_OK) return rc;
+  if (elapsed_cycles) {
+    elapsed_cycles[0] = c[0];
+    elapsed_cycles[1] = c[1];
+  }
+  return spec_verify_get_error(h, nullptr);
 }
 
 int spec_verify_info(spec_verify_t h, int* cluster_size, int* n_clusters, int* rounds, int* tma, int* launches_per_call) {

@@ -55,6 +55,7 @@ def test_host_side_argument_checks(lib):
     assert lib.spec_verify(None, 1, *([None] * 11)) == sv.SV_ERR_ARG
     assert lib.spec_verify_tv(None, 1, *([None] * 5)) == sv.SV_ERR_ARG
     assert lib.spec_verify_get_error(None, None) == sv.SV_ERR_ARG
+    assert lib.spec_verify_selftest_wait(None, 1, None) == sv.SV_ERR_ARG
     lib.spec_verify_destroy(None)
     assert lib.spec_verify_strerror(0) == b"ok"
     assert b"invalid" in lib.spec_verify_strerror(6)

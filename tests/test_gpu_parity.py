@@ -172,6 +172,27 @@ def test_host_entry_point_larger_batch(lib):
     v.close()
 
 
+def test_host_entry_point_pageable(lib):
+    """Pageable host logits go through the device staging copy; page-locked
+    ones are read in place by the kernels.  Both equal the device path."""
+    w = si.C3_T06.scaled(batch=6)
+    b = si.generate(w)
+    dev, _, _ = run_gpu(lib, w, b)
+    v = lib.SpecVerifier(w.batch, w.k, w.vocab, torch.bfloat16, flags=lib.SV_FLAG_HOST_STAGING)
+    tg = torch.from_numpy(b.target.view(np.int16)).view(torch.bfloat16)
+    dr = torch.from_numpy(b.draft.view(np.int16)).view(torch.bfloat16)
+    assert not tg.is_pinned() and not dr.is_pinned()
+    for pinned in (False, True):
+        host_out = v.alloc_outputs(w.batch, want_pq=True, want_tv=True, device="cpu")
+        args = (tg.pin_memory(), dr.pin_memory()) if pinned else (tg, dr)
+        v.verify_host(*args, torch.from_numpy(b.tokens), torch.from_numpy(b.temperature),
+                      torch.from_numpy(b.uniforms), host_out)
+        torch.cuda.synchronize()
+        for key in dev:
+            assert np.array_equal(dev[key], host_out[key].numpy(), equal_nan=True), (pinned, key)
+    v.close()
+
+
 def test_empty_batch_and_bad_args(lib):
     v = lib.SpecVerifier(4, 3, 64, torch.float32)
     e = torch.empty((0, 4, 64), device="cuda")
