@@ -130,8 +130,8 @@ struct Small {
   unsigned long long bar;      // stage mbarrier
   unsigned long long xbar[2];  // exchange mbarriers, one per slot set (peers complete their bytes)
   unsigned cnt;                // warps done copying the current stage
-  float gz_t, gz_d;            // logits at the drafted token (thread 0 of the owner CTA)
-  int pad0;
+  float gz_t, gz_d;            // logits at the drafted token (thread 0 of the owner CTA; lazy: of every CTA)
+  float gz_u;                  // lazy verification: the uniform of the accept test
   X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
   Merged mg[2];                // merged row statistics (warp 0 to the other warps), per slot set
 };
@@ -578,6 +578,12 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     }
   }
 
+  if (LAZY && PAIR && tid == 0) {   // parked in shared memory, out of the registers pass A needs
+    S.gz_t = lz_t;
+    S.gz_d = lz_d;
+    S.gz_u = lz_u;
+  }
+
   const bool t_ok = T >= 0.0f && T <= 3.0e38f;   // false for NaN and inf
   const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
   const bool x_ok = !PAIR || P.tv_only || (x >= 0 && x < V);
@@ -730,8 +736,8 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
         if (greedy) {
           cont = x == A_t;
         } else {
-          const float lpx = fmaf(lz_t, c, -R_t), lqx = fmaf(lz_d, c, -R_d);
-          cont = lz_u < exp2f(lpx - lqx) * (S_d / S_t);
+          const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
+          cont = S.gz_u < exp2f(lpx - lqx) * (S_d / S_t);
         }
       }
       Merged m;
@@ -944,26 +950,38 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   const int k = F.k, items = F.items;
   const size_t ub = (size_t)b * (k + 1);
   const int npos = F.tv_only ? k : k + 1;
-  // accept bits (not written, and not used, for TV only)
+  // Everything that does not depend on tau is loaded first, together: the
+  // accept bits (not written, and not used, for TV only), the statistics and
+  // greedy token of every unit (lane i holds position i's), the drafted
+  // tokens and the uniform of the final draw.
   const int a = lane < k ? F.ws_acc[(size_t)b * k + lane] : 1;
+  UnitStat sl;
+  sl.c = 0.0f; sl.R_t = 0.0f; sl.R_d = 0.0f; sl.r = 0.0f; sl.S_t = 1.0f; sl.status = 0; sl.greedy = 0; sl.pad = 0;
+  int yl = 0;
+  if (lane < npos) {
+    sl = F.ws_stat[ub + lane];
+    yl = F.ws_y[ub + lane];
+  }
+  const int tok = !F.tv_only && lane < k ? F.tokens[(size_t)b * k + lane] : -1;
+  const float u_fin = F.tv_only ? 0.0f : F.uniforms[ub + k];   // the final draw uses u[b, k]
+
   const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
   const int tau = rej ? __ffs(rej) - 1 : k;
   // the last position whose unit was verified: a lazy walk stopped at the first rejection
   const int last = F.lazy ? tau : npos - 1;
-  const int st = lane < npos && lane <= last ? F.ws_stat[ub + lane].status : 0;
-  const bool bad = __any_sync(FULL, st != 0);
+  const bool bad = __any_sync(FULL, lane <= last && sl.status != 0);
 
   // TV of every valid, non-greedy position: 8 positions per pass, 4 lanes per
   // position, each lane adding 16 consecutive range masses (loaded together)
   if (F.out_tv) {
     for (int i0 = 0; i0 < k; i0 += 8) {
       const int i = i0 + (lane >> 2), q = lane & 3;
-      float v = 0.0f, S_t = 1.0f;
-      bool ok = false;
+      const int src = min(i, k - 1);   // every lane takes part in the shuffles
+      const int st_i = __shfl_sync(FULL, sl.status, src), gr_i = __shfl_sync(FULL, sl.greedy, src);
+      const float S_t = __shfl_sync(FULL, sl.S_t, src);
+      const bool ok = i < k && st_i == 0 && !gr_i;
+      float v = 0.0f;
       if (i < k) {
-        const UnitStat us = F.ws_stat[ub + i];
-        ok = us.status == 0 && !us.greedy;
-        S_t = us.S_t;
         const float4* w4 = reinterpret_cast<const float4*>(F.ws_w + (ub + i) * ITEMS_MAX) + q * 4;
         float4 w[4];
 #pragma unroll
@@ -989,10 +1007,15 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   }
   const bool pair = tau < k;
   const size_t uu = ub + tau;
-  const UnitStat us = F.ws_stat[uu];
+  UnitStat us;   // unit tau's statistics, from lane tau
+  us.c = __shfl_sync(FULL, sl.c, tau); us.R_t = __shfl_sync(FULL, sl.R_t, tau);
+  us.R_d = __shfl_sync(FULL, sl.R_d, tau); us.r = __shfl_sync(FULL, sl.r, tau);
+  us.S_t = __shfl_sync(FULL, sl.S_t, tau); us.status = 0; us.pad = 0;
+  us.greedy = __shfl_sync(FULL, sl.greedy, tau);
+  const int y_greedy = __shfl_sync(FULL, yl, tau);
   int y = 0;
   if (us.greedy) {
-    y = F.ws_y[uu];
+    y = y_greedy;
   } else {
     // ---- which (CTA, warp) range holds u * total mass
     const float* wp = F.ws_w + uu * ITEMS_MAX;
@@ -1014,7 +1037,7 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
     double excl = __shfl_up_sync(FULL, incl, 1);
     if (lane == 0) excl = 0.0;
     const double total = __shfl_sync(FULL, incl, 31);
-    const double tt = (double)F.uniforms[ub + k] * total;   // the final draw uses u[b, k]
+    const double tt = (double)u_fin * total;
     const bool ca = wa > 0.0 && tt < excl + wa;
     const bool cb = wb > 0.0 && tt < incl;
     const unsigned hit = __ballot_sync(FULL, ca || cb);
@@ -1109,12 +1132,7 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
     estar = __shfl_sync(FULL, estar, lstar);
     y = (int)slice0 + (vbeg + jstar * 32 + lstar) * EPV + estar;
   }
-  if (lane <= k) {
-    int tok = -1;
-    if (lane < tau) tok = F.tokens[(size_t)b * k + lane];
-    else if (lane == tau) tok = y;
-    F.out_tokens[ub + lane] = tok;
-  }
+  if (lane <= k) F.out_tokens[ub + lane] = lane < tau ? tok : lane == tau ? y : -1;
   if (lane == 0) F.out_tau[b] = tau;
 }
 
