@@ -153,8 +153,8 @@ int spec_verify_loss_grad(spec_verify_t h, int batch,
 
 /* spec_verify, and also the entropy of every logit row's distribution, in
  * the same pass over the logits.  The pages tie the fall of acceptance to
- * fluctuations in the model's output entropy, "how spread out the token
- * probabilities are" ("Optimizing speculative decoding" and "GLM-5.2: Tuning
+ * fluctuations in the entropy of the model's output, i.e. in how widely its
+ * probability mass is spread ("Optimizing speculative decoding" and "GLM-5.2: Tuning
  * MTP speculative decoding to the limit", section "Rejection sampling and a
  * loss that optimizes acceptance directly"); the statistic here is the
  * Shannon entropy, in nats, of p = softmax(z / T), the distribution the

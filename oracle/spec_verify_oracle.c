@@ -6,25 +6,27 @@
  * CPU-baseline leg load it.  It shares no code with the CUDA library (no
  * header, no helper, no table) and the library never calls it.
  *
- * Sources.  Page 1 = "Optimizing speculative decoding" (longformexplainers,
- * llm-inference/21), page 2 = "GLM-5.2: Tuning MTP speculative decoding to
- * the limit", page 3 = "DSpark for GLM-5.2" (makora blog).
+ * Sources (web pages, by title):
  *   - Drafts are sampled from the draft distribution and accepted or rejected
- *     against the target distribution, which the protocol preserves: page 1
- *     and page 2, section "Rejection sampling and a loss that optimizes
- *     acceptance directly", first bullet.
+ *     against the target distribution, which the protocol preserves:
+ *     "Optimizing speculative decoding" and "GLM-5.2: Tuning MTP speculative
+ *     decoding to the limit", section "Rejection sampling and a loss that
+ *     optimizes acceptance directly", first bullet.
  *   - The per-token acceptance probability of lossless speculative sampling is
- *     sum_x min(p(x), q(x)): page 1, section "Kimi K3".
+ *     sum_x min(p(x), q(x)): "Optimizing speculative decoding", section
+ *     "Kimi K3".
  *   - Total variation is half the sum of absolute probability differences:
- *     page 1, same section as the first item, second bullet.
+ *     "Optimizing speculative decoding", same section as the first item,
+ *     second bullet.
  *   - The target verifies the whole k-token chain in one forward pass, i.e.
- *     it provides k+1 target distributions: page 1, "The draft model moved
- *     inside".  Accepted length tau: page 3, introduction.
- *   - Page 3 cites Leviathan, Kalman and Matias (ICML 2023) as the origin of
- *     the scheme.  The pages do not print the residual distribution
- *     max(0, p - q) or the bonus draw; they are the only completion consistent
- *     with both "preserves the target distribution" and "acceptance =
- *     sum min(p, q)", and are taken in that reading.
+ *     it provides k+1 target distributions: "Optimizing speculative
+ *     decoding", section "The draft model moved inside".  Accepted length
+ *     tau: "DSpark for GLM-5.2", introduction.
+ *   - "DSpark for GLM-5.2" cites Leviathan, Kalman and Matias (ICML 2023) as
+ *     the origin of the scheme.  The pages do not print the residual
+ *     distribution max(0, p - q) or the bonus draw; they are the only
+ *     completion under which the target distribution is preserved and the
+ *     acceptance equals sum min(p, q), and are taken in that reading.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - temperature: p = softmax(z / T) for the target and q = softmax(z / T) for
@@ -296,10 +298,11 @@ int so_verify_chain(const so_chain_in* in, so_chain_out* out) {
 
 /* Entropy, in nats, of one row's distribution at temperature T:
  *   H = -sum_j p_j log p_j,  p = softmax(z / T).
- * The pages tie acceptance degradation to fluctuations in the model's output
- * entropy, "how spread out the token probabilities are" (page 1 and page 2,
- * section "Rejection sampling and a loss that optimizes acceptance
- * directly"); they print no formula, and Shannon entropy of the distribution
+ * The pages tie acceptance degradation to fluctuations in the entropy of the
+ * model's output, i.e. in how widely its probability mass is spread
+ * ("Optimizing speculative decoding" and "GLM-5.2: Tuning MTP speculative
+ * decoding to the limit", section "Rejection sampling and a loss that
+ * optimizes acceptance directly"); they print no formula, and Shannon entropy of the distribution
  * the verifier uses is the reading.  Entries with p_j = 0 (logit -inf) add
  * nothing (0 log 0 = 0).  T == 0: the greedy one-hot distribution, H = 0.
  * NaN for a temperature that is NaN, infinite or negative, or a row whose
@@ -366,12 +369,14 @@ int so_entropy_batch(int64_t B, int32_t k, int64_t V, int32_t dtype, const void*
  * draft logits (the target is frozen).  For one position with target row zt,
  * draft row zd and temperature T > 0, p = softmax(zt / T), q = softmax(zd / T):
  *   alpha = sum_x min(p(x), q(x)), the probability that the protocol accepts
- *           the drafted token (page 1, section "Kimi K3"), = 1 - TV;
- *   kind 0, TV loss:       l = TV = 1 - alpha  (page 1 and page 2, section
- *           "Rejection sampling and a loss that optimizes acceptance
- *           directly", second bullet; per position is the reading);
- *   kind 1, overlap loss:  l = -ln alpha  (page 1, section "Kimi K3": the
- *           negative log of the draft-target overlap).
+ *           the drafted token ("Optimizing speculative decoding", section
+ *           "Kimi K3"), = 1 - TV;
+ *   kind 0, TV loss:       l = TV = 1 - alpha  ("Optimizing speculative
+ *           decoding" and "GLM-5.2: Tuning MTP speculative decoding to the
+ *           limit", section "Rejection sampling and a loss that optimizes
+ *           acceptance directly", second bullet; per position is the reading);
+ *   kind 1, overlap loss:  l = -ln alpha  ("Optimizing speculative decoding",
+ *           section "Kimi K3": the negative log of the draft-target overlap).
  * With weight w the position contributes w * l to the loss, and
  *   d(w l)/d zd_m = w * dl/dalpha * (q_m / T) * ([q_m < p_m] - beta),
  *   beta = sum_x [q_x < p_x] q_x,
