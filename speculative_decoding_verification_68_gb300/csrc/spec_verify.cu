@@ -106,6 +106,8 @@ struct KParams {
   void* grad;                // [B, k, V] in the logit dtype
   int loss_kind;             // SV_LOSS_TV or SV_LOSS_OVERLAP
   int grad_vec;              // gradient rows can take 16-byte stores
+  // lazy verification
+  int* ws_grab;              // chains handed out so far past the static ones (zeroed before the launch)
 };
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
@@ -124,6 +126,7 @@ struct alignas(16) Merged {
   int IR_t;            // R_t as an integer (NO_REF if the row has no finite maximum)
   int status;          // ST_* bits, 0 if valid
   int cont;            // lazy verification: the chain goes on to the next position
+  int grab;            // lazy verification: the counter value rank 0 drew for this unit (-1: none)
 };
 
 struct Small {
@@ -133,6 +136,7 @@ struct Small {
   float gz_t, gz_d;            // logits at the drafted token (thread 0 of the owner CTA; lazy: of every CTA)
   float gz_u;                  // lazy verification: the uniform of the accept test
   X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
+  int grab[2];                 // lazy verification: rank 0's counter value, per slot set
   Merged mg[2];                // merged row statistics (warp 0 to the other warps), per slot set
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "bookkeeping area too small");
@@ -160,6 +164,10 @@ __device__ __forceinline__ void st_async_x1(uint32_t slot, const X1& v, uint32_t
                "r"(__float_as_uint(v.s_d)), "r"(rbar) : "memory");
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
                ::"r"(slot + 16), "r"(v.i_t), "r"(v.i_d), "r"(v.ref_t), "r"(v.ref_d), "r"(rbar) : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t slot, int v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(slot), "r"(v), "r"(rbar)
+               : "memory");
 }
 __device__ __forceinline__ void mbar_init(uint32_t a, unsigned n) { asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory"); }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, unsigned bytes) {
@@ -515,7 +523,7 @@ template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
 __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
-                                             const float T, const int x) {
+                                             const float T, const int x, const bool carry = false) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -530,6 +538,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     lz_d = Lay<Tl>::load_scalar(P.draft, ((long long)b * k + ipos) * V + x);
     lz_u = P.uniforms[(size_t)b * (k + 1) + ipos];
   }
+  // A unit that carries a grab: rank 0 draws the next counter value now and
+  // sends it to every CTA with this unit's exchange.
+  int grab_v = 0;
+  if (LAZY && carry && tid == 0 && g.rank() == 0) grab_v = atomicAdd(P.ws_grab, 1);
 
   // ---------------- this warp's vectors of the unit into registers
   uint4 rt[R], rd[R];
@@ -648,9 +660,13 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   }
   const int set1 = n1 & 1;
   const uint32_t xbar = saddr(&S.xbar[set1]);
-  if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items() * 32u);
+  if (tid == 0) mbar_expect_tx(xbar, (unsigned)g.items() * 32u + (LAZY && carry ? 4u : 0u));
   if (lane < (int)g.C())
     st_async_x1(peer_addr(saddr(&S.x1[set1][g.rank() * NWARP + warp]), lane), mine, peer_addr(xbar, lane));
+  if (LAZY && carry && warp == 0 && g.rank() == 0) {   // cluster-uniform condition
+    const int gv = __shfl_sync(FULL, grab_v, 0);
+    if (lane < (int)g.C()) st_async_b32(peer_addr(saddr(&S.grab[set1]), lane), gv, peer_addr(xbar, lane));
+  }
   const unsigned xpar = (unsigned)((n1 >> 1) & 1);
   ++n1;
 
@@ -742,6 +758,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       }
       Merged m;
       m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
+      m.grab = LAZY && carry ? S.grab[set1] : -1;
       mg = m;
       if (g.rank() == 0) {
         UnitStat st;
@@ -840,23 +857,27 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
   if constexpr (LAZY) {
-    // Each cluster walks its chains b = cluster_id, cluster_id + n_clusters,
-    // ... position by position and stops a chain at its first rejection (or
-    // after its bonus row).  Two chains are in flight, taking turns, so that
-    // the unit after the current one is always known (the other chain's next
-    // position, decided one unit earlier) and its copy can be issued ahead.
-    // The walk is the same in every CTA of the cluster: it depends only on
-    // the accept decisions, which every CTA takes from the merged statistics.
-    unsigned jn = 0;   // the next chain of this cluster's list to start
-    auto take = [&]() {
-      Unit t;
-      t.ipos = 0;
-      t.b = -1;
-      if (cid + (unsigned long long)jn * ncl < B) { t.b = (int)(cid + jn * ncl); ++jn; }
-      return t;
-    };
-    Unit cur = take(), nxt = take();
-    bool loaded = false;   // cur's copy was issued while the previous unit ran
+    // Each cluster walks chains position by position and stops a chain at its
+    // first rejection (or after its bonus row).  Two chains are in flight,
+    // taking turns, so that the unit after the current one is always known
+    // (the other chain's next position, decided one unit earlier) and its
+    // copy can be issued ahead.  A third chain waits in reserve.
+    // Chains are handed out at run time: each cluster starts with chains
+    // cluster_id + j * n_clusters, j < 3; when the reserve is taken, the next
+    // unit's exchange carries a value of a global counter that rank 0 bumps,
+    // and chain 3 * n_clusters + value becomes the reserve.  The walk is the
+    // same in every CTA of the cluster: it depends only on the accept
+    // decisions, which every CTA takes from the merged statistics, and on the
+    // counter values, which every CTA receives.
+    const unsigned first = 3u * ncl;
+    auto chain_or_none = [&](unsigned long long c) { return c < B ? (int)c : -1; };
+    Unit cur, nxt;
+    cur.b = chain_or_none(cid); cur.ipos = 0;
+    nxt.b = chain_or_none(cid + (unsigned long long)ncl); nxt.ipos = 0;
+    int reserve = chain_or_none(cid + 2ull * ncl);
+    bool refill = false;      // the reserve was taken: the next unit carries a grab
+    bool exhausted = cid + 2ull * ncl >= B;
+    bool loaded = false;      // cur's copy was issued while the previous unit ran
     while (cur.b >= 0) {
       if (P.tma && !loaded) {   // nothing issued ahead: every warp is done with the stage
         __syncthreads();
@@ -865,15 +886,27 @@ __global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
       const bool has_next = nxt.b >= 0;
       const float T = P.temperature[cur.b];
       const int x = cur.ipos < k ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
+      const bool carry = refill;
       int cont;
       if (cur.ipos < k)
-        cont = process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt, P.tma && has_next, T, x);
+        cont = process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
+                                                     P.tma && has_next, T, x, carry);
       else
-        cont = process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt, P.tma && has_next, T, x);
+        cont = process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
+                                                      P.tma && has_next, T, x, carry);
       phase ^= 1u;
+      if (carry) {   // this unit's exchange brought the new reserve
+        reserve = chain_or_none(first + (unsigned long long)(unsigned)S.mg[(n1 - 1) & 1].grab);
+        exhausted = reserve < 0;
+        refill = false;
+      }
       Unit after;
-      if (cont) { after.b = cur.b; after.ipos = cur.ipos + 1; }
-      else after = take();
+      if (cont) {
+        after.b = cur.b; after.ipos = cur.ipos + 1;
+      } else {
+        after.b = reserve; after.ipos = 0;
+        if (reserve >= 0) { reserve = -1; refill = !exhausted; }
+      }
       if (has_next) { cur = nxt; nxt = after; loaded = true; }
       else { cur = after; loaded = false; }
     }
@@ -1300,7 +1333,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
         Merged m;
         m.S_t = S_t; m.S_d = S_d;
         m.R_t = IR_t == NO_REF ? 0.0f : (float)IR_t; m.R_d = IR_d == NO_REF ? 0.0f : (float)IR_d;
-        m.r = row_ok ? S_t / S_d : 0.0f; m.IR_t = IR_t; m.status = row_ok ? 0 : ST_ROW; m.cont = 0;
+        m.r = row_ok ? S_t / S_d : 0.0f; m.IR_t = IR_t; m.status = row_ok ? 0 : ST_ROW; m.cont = 0; m.grab = -1;
         mg = m;
       }
       __syncwarp();
@@ -1510,6 +1543,7 @@ struct spec_verify_ctx {
   FusedFn kernel_grad;       // loss-gradient kernel
   int n_clusters_grad;
   FusedFn kernel_lazy;       // lazy verification (each chain up to its first rejection)
+  int* ws_grab;              // lazy verification: chain hand-out counter
   int n_clusters_lazy;
   FinalFn finalize;
   int32_t* ws_acc;
@@ -1538,7 +1572,7 @@ static constexpr int TIMING_RING = 4096;
 
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
-  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
+  void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->ws_grab, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
                   h->st_unif, h->st_out_tokens, h->st_out_tau, h->st_out_p, h->st_out_q, h->st_out_tv};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -1796,7 +1830,8 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
             cudaMalloc(&h->ws_stat, mb * (k + 1) * sizeof(UnitStat)) == cudaSuccess &&
             cudaMalloc(&h->ws_w, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&h->ws_p, mb * (k + 1) * ITEMS_MAX * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess;
+            cudaMalloc(&h->d_flags, 4 * sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&h->ws_grab, sizeof(int)) == cudaSuccess;
   if (ok && (flags & SV_FLAG_HOST_STAGING)) {
     const size_t rowb = (size_t)vocab * es;
     ok = cudaMalloc(&h->st_target, mb * (k + 1) * rowb) == cudaSuccess &&
@@ -1902,6 +1937,8 @@ int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, cons
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
+  P.ws_grab = h->ws_grab;
+  if (cudaMemsetAsync(h->ws_grab, 0, sizeof(int), s) != cudaSuccess) return SV_ERR_CUDA;
   const int rc = launch_fused(h, P, batch, s, false, true);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s, true);
