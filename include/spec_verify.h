@@ -119,8 +119,9 @@ int spec_verify(spec_verify_t h, int batch,
  * There is no p, q or TV output (positions after the stop are not
  * evaluated), and accepted positions skip the residual pass.  Two kernel
  * launches: one walks every chain position by position up to its stop
- * (each cluster of CTAs takes its share of the chains, two at a time), then
- * the finalize kernel draws the final tokens. */
+ * (each cluster of CTAs works on two chains at a time and takes the next
+ * chain from a shared counter when one stops), then the finalize kernel
+ * draws the final tokens. */
 int spec_verify_lazy(spec_verify_t h, int batch,
                      const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, const float* temperature, const float* uniforms,
