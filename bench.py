@@ -162,8 +162,15 @@ def cpu_baseline(w: si.Workload, target_seconds: float = 10.0):
         orc.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, want_tv=w.want_tv, nthreads=cores)
         dt = time.perf_counter() - t
         nb = nb2
+    # the same oracle on one thread, over a few chains (about 1/8 of the time above)
+    n1 = max(1, min(nb, int(nb * 0.125 * min(1.0, 16.0 / cores) + 0.5)))
+    b1 = si.generate(w, 0, n1)
+    t = time.perf_counter()
+    orc.verify(b1.target, b1.draft, b1.tokens, b1.temperature, b1.uniforms, w.dtype, want_tv=w.want_tv, nthreads=1)
+    dt1 = time.perf_counter() - t
     return {"value": nb * w.k / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{nb} of {w.batch} chains of {w.name} (fp64 C oracle, {cores} threads), {dt:.2f} s"}
+            "sample": f"{nb} of {w.batch} chains of {w.name} (fp64 C oracle, {cores} threads), {dt:.2f} s",
+            "single_thread": {"value": n1 * w.k / dt1, "sample": f"{n1} chains on 1 thread, {dt1:.2f} s"}}
 
 
 def reference_arm(args, w: si.Workload, rank: int):
