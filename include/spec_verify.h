@@ -41,7 +41,9 @@
  *   - A handle is not thread-safe; use one handle per stream.
  *   - Uniforms are in [0, 1); the seeded generator used by this project
  *     produces them on the 2^-24 lattice.
- *   - Limits: 1 <= k <= 31; V <= 163840 (bf16) or 81920 (fp32).
+ *   - Limits: 1 <= k <= 31; V <= 327680 (bf16) or 163840 (fp32).  Above
+ *     163840 (bf16) or 81920 (fp32) the kernels hold twice the registers per
+ *     thread and run one CTA per SM instead of two.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H

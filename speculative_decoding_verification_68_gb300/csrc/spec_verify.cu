@@ -823,7 +823,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
 }
 
 template <typename Tl, int R, bool ENT, bool LAZY>
-__global__ void __launch_bounds__(NT, 2) sv_fused_kernel(const KParams P) {
+__global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   Small& S = *reinterpret_cast<Small*>(smem);
   unsigned char* stage = smem + SMALL_BYTES;   // [2 rows][NWARP][R*32] vectors
@@ -1449,7 +1449,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
 }
 
 template <typename Tl, int R>
-__global__ void __launch_bounds__(NT, 2) sv_grad_kernel(const KParams P) {
+__global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_grad_kernel(const KParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ GradStat gs[2];
   Small& S = *reinterpret_cast<Small*>(smem);
@@ -1494,8 +1494,10 @@ __global__ void __launch_bounds__(NT, 2) sv_grad_kernel(const KParams P) {
 
 typedef void (*FusedFn)(const KParams);
 typedef void (*FinalFn)(const FParams);
-constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10};
-constexpr int N_R = 6;
+// Register rounds per thread.  Up to 10 two CTAs share an SM; 16 and 20 (the
+// largest vocabularies) run one CTA per SM, with the register file to itself.
+constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10, 16, 20};
+constexpr int N_R = 8;
 
 template <typename Tl>
 FusedFn pick_grad(int r) {
@@ -1505,7 +1507,9 @@ FusedFn pick_grad(int r) {
     case 4: return sv_grad_kernel<Tl, 4>;
     case 6: return sv_grad_kernel<Tl, 6>;
     case 8: return sv_grad_kernel<Tl, 8>;
-    default: return sv_grad_kernel<Tl, 10>;
+    case 10: return sv_grad_kernel<Tl, 10>;
+    case 16: return sv_grad_kernel<Tl, 16>;
+    default: return sv_grad_kernel<Tl, 20>;
   }
 }
 
@@ -1524,7 +1528,9 @@ void pick_kernels(int r, FusedFn& f, FusedFn& fe, FusedFn& fl, FinalFn& g) {
     case 4: pick_r<Tl, 4>(f, fe, fl, g); break;
     case 6: pick_r<Tl, 6>(f, fe, fl, g); break;
     case 8: pick_r<Tl, 8>(f, fe, fl, g); break;
-    default: pick_r<Tl, 10>(f, fe, fl, g); break;
+    case 10: pick_r<Tl, 10>(f, fe, fl, g); break;
+    case 16: pick_r<Tl, 16>(f, fe, fl, g); break;
+    default: pick_r<Tl, 20>(f, fe, fl, g); break;
   }
 }
 

@@ -46,10 +46,9 @@ def test_host_side_argument_checks(lib):
     assert lib.spec_verify_init(ctypes.byref(h), 1, 0, 100, 0, 0) == 3      # k = 0
     assert lib.spec_verify_init(ctypes.byref(h), 1, 32, 100, 0, 0) == 3     # k above 31
     assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 100, 9, 0) == 2      # dtype
-    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 200000, 1, 0) == 3   # vocabulary too large
-    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 163841, 1, 0) == 3   # bf16: V <= 163,840
-    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 81921, 0, 0) == 3    # fp32: V <= 81,920
-    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 151552, 0, 0) == 3
+    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 400000, 1, 0) == 3   # vocabulary too large
+    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 327681, 1, 0) == 3   # bf16: V <= 327,680
+    assert lib.spec_verify_init(ctypes.byref(h), 1, 7, 163841, 0, 0) == 3   # fp32: V <= 163,840
     assert lib.spec_verify_init(ctypes.byref(h), -1, 7, 100, 0, 0) == sv.SV_ERR_ARG
     assert lib.spec_verify_init(ctypes.byref(h), 1 << 28, 7, 100, 0, 0) == 3   # B*(k+1) reaches 2^31
     assert lib.spec_verify_ex(None, 1, *([None] * 13)) == sv.SV_ERR_ARG

@@ -75,7 +75,8 @@ def test_entropy_workloads(lib, oracle, w):
     check(lib, oracle, w)
 
 
-@pytest.mark.parametrize("V,dtype", [(16, si.FP32), (1001, si.FP32), (2050, si.BF16), (32001, si.BF16), (163840, si.BF16)])
+@pytest.mark.parametrize("V,dtype", [(16, si.FP32), (1001, si.FP32), (2050, si.BF16), (32001, si.BF16), (163840, si.BF16),
+                                     (262144, si.BF16), (151552, si.FP32)])
 def test_entropy_ragged(lib, oracle, V, dtype):
     w = si.Workload(f"ent_V{V}", 5, 4, V, dtype, 2.0, draft_sigma=0.8, temp_mode=1, temp_lo=0.3, temp_hi=1.5)
     check(lib, oracle, w)

@@ -57,7 +57,7 @@ def test_lazy_matches_full_and_oracle(lib, oracle, w):
     print(w.name, stats, "mean tau", float(lazy["tau"].mean()))
 
 
-@pytest.mark.parametrize("V,dtype", [(37, si.FP32), (2050, si.BF16), (32001, si.BF16)])
+@pytest.mark.parametrize("V,dtype", [(37, si.FP32), (2050, si.BF16), (32001, si.BF16), (262144, si.BF16), (151552, si.FP32)])
 def test_lazy_ragged(lib, oracle, V, dtype):
     w = si.Workload(f"lazy_V{V}", 9, 5, V, dtype, 2.0, draft_sigma=0.4, temp_mode=1, temp_lo=0.0, temp_hi=1.5)
     b = si.generate(w)

@@ -116,6 +116,16 @@ def test_loss_grad_ragged_and_weights(lib, oracle, V, dtype):
     check(lib, oracle, w, "overlap", weights=wts)
 
 
+@pytest.mark.parametrize("kind", ["tv", "overlap"])
+@pytest.mark.parametrize("V,dtype", [(262144, si.BF16), (151552, si.FP32)])
+def test_loss_grad_large_vocab(lib, oracle, V, dtype, kind):
+    """Vocabularies past 163,840 (bf16) or 81,920 (fp32): one CTA per SM.  The
+    draft noise keeps near-tie positions (left out of the comparison) rare."""
+    w = si.Workload(f"lg_big_V{V}", 4, 3, V, dtype, 2.0, draft_sigma=1.5, temp_mode=1, temp_lo=0.4, temp_hi=1.5)
+    wts = np.random.default_rng(V).uniform(0.2, 3.0, (4, 3)).astype(np.float32)
+    check(lib, oracle, w, kind, weights=wts)
+
+
 def test_loss_grad_invalid_and_identical(lib, oracle):
     w = si.Workload("lg_special", 6, 3, 4096, si.BF16, 2.0, draft_sigma=0.5, temp_lo=1.0, temp_hi=1.0)
     b = si.generate(w)

@@ -67,6 +67,14 @@ def test_ragged_vocab(lib, oracle, V, dtype, T):
     check(lib, oracle, w)
 
 
+# -------- vocabularies past 163,840 (bf16) or 81,920 (fp32): twice the register rounds, one CTA per SM
+@pytest.mark.parametrize("V,dtype", [(163848, si.BF16), (200003, si.BF16), (262144, si.BF16), (327680, si.BF16),
+                                     (81928, si.FP32), (151552, si.FP32), (163840, si.FP32)])
+def test_large_vocab(lib, oracle, V, dtype):
+    w = si.Workload(f"bigV{V}", 5, 3, V, dtype, 2.0, draft_sigma=0.6, temp_mode=1, temp_lo=0.0, temp_hi=1.3)
+    check(lib, oracle, w)
+
+
 @pytest.mark.parametrize("k", [1, 2, 15, 31])
 def test_draft_lengths(lib, oracle, k):
     w = si.Workload(f"k{k}", 5, k, 3000, si.BF16, 1.0, draft_sigma=0.3, temp_mode=1, temp_lo=0.5, temp_hi=1.5)
@@ -202,7 +210,7 @@ def test_empty_batch_and_bad_args(lib):
     with pytest.raises(lib.SpecVerifyError):
         lib.SpecVerifier(4, 32, 64, torch.float32)     # k above the limit
     with pytest.raises(lib.SpecVerifyError):
-        lib.SpecVerifier(4, 7, 200000, torch.bfloat16)  # V above the limit
+        lib.SpecVerifier(4, 7, 327681, torch.bfloat16)  # V above the limit
     v.close()
 
 

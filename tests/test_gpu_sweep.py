@@ -22,7 +22,7 @@ def _cases(n=12, seed=2026):
         B = int(rng.integers(1, 25))
         if B * (2 * k + 1) * V > 40_000_000:
             continue
-        dtype = si.BF16 if rng.random() < 0.6 or V > 81920 else si.FP32   # fp32 rows: V <= 81,920
+        dtype = si.BF16 if rng.random() < 0.6 or V > 81920 else si.FP32
         temp_mode = int(rng.integers(0, 2))
         lo = float(rng.choice([0.0, 0.5, 1.0])) if temp_mode == 0 else 0.2
         w = si.Workload(f"sweep{len(out)}_B{B}_k{k}_V{V}", B, k, V, dtype, float(rng.uniform(0.5, 4.0)),
