@@ -418,6 +418,22 @@ def main(argv=None):
                                         "api": "spec_verify_tv (TV of every position only)"}
         so.close()
         del di, oo, bo, otv
+        # a 262,144-token vocabulary (register rounds 16, one CTA per SM), independent drafts, TV on
+        wo = si.Workload("b128_k7_v262144_bf16_indep_tv", 128, 7, 262144, si.BF16, 2.0, draft_mode=1,
+                         draft_sigma=2.0, want_tv=True)
+        bo = si.generate(wo)
+        di = device_batch(bo, device)
+        so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16", flags=svlib.SV_FLAG_KERNEL_TIMING)
+        oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device)
+        for _ in range(3):
+            so.verify(*di, out=oo)
+        kms, kto = measure_kernel(so, di, oo, 20, flush=flush)
+        ob = wo.logit_bytes
+        others[wo.name] = {"kernel_us": 1e3 * kms, "kernel_us_spread": spread_us(kto),
+                           "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3), "gbps": ob / (kms / 1e3) / 1e9,
+                           "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak, "launch": so.info()}
+        so.close()
+        del di, oo, bo
         # lazy verification (no TV): whole call timed with events; its bytes are the rows
         # actually read, (tau + 1) row pairs per chain, or k pairs and the bonus row
         for wo in (si.C3_T1, si.C4, w0 if w0.batch <= 1024 else w0.scaled(batch=1024)):
