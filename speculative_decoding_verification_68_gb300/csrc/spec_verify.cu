@@ -9,7 +9,8 @@
 //     vocabulary slice [r*Vs, (r+1)*Vs) of both rows, and warp w of the CTA a
 //     contiguous range of WV 16-byte vectors of that slice.
 //   * The kernel is persistent: each cluster walks units cluster_id,
-//     cluster_id + n_clusters, ...  Two CTAs share an SM.  Each CTA has one
+//     cluster_id + n_clusters, ...  Two CTAs share an SM (one, for the
+//     largest vocabularies, which need twice the registers).  Each CTA has one
 //     shared-memory stage; a bulk (TMA) copy lands the next unit's slice there
 //     while the current unit is processed from registers.  The last warp to
 //     copy its part out of the stage issues the next copy.
@@ -1494,8 +1495,8 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_grad_kernel(const KPar
 
 typedef void (*FusedFn)(const KParams);
 typedef void (*FinalFn)(const FParams);
-// Register rounds per thread.  Up to 10 two CTAs share an SM; 16 and 20 (the
-// largest vocabularies) run one CTA per SM, with the register file to itself.
+// Register rounds per thread.  Up to 10, two CTAs share an SM; at 16 and 20
+// (the largest vocabularies) one CTA has the SM's register file to itself.
 constexpr int R_CHOICES[] = {1, 2, 4, 6, 8, 10, 16, 20};
 constexpr int N_R = 8;
 
