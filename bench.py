@@ -220,6 +220,9 @@ def measure_kernel(sv, dev_inputs, out, steps, flush=None):
     return statistics.mean(kt), kt
 
 
+REPS = 50   # timed calls per per_workload entry, L2 flushed before each
+
+
 def spread_us(kt):
     """p10 / p50 / p90 of kernel durations given in ms, in microseconds."""
     q = np.percentile(np.asarray(kt, dtype=np.float64) * 1e3, [10, 50, 90])
@@ -376,8 +379,8 @@ def main(argv=None):
             oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device)
             for _ in range(3):
                 so.verify(*di, out=oo)
-            kms, kto = measure_kernel(so, di, oo, 20, flush=flush)
-            kms_warm, _ = measure_kernel(so, di, oo, 20)   # no flush: inputs below L2 size stay resident
+            kms, kto = measure_kernel(so, di, oo, REPS, flush=flush)
+            kms_warm, _ = measure_kernel(so, di, oo, REPS)   # no flush: inputs below L2 size stay resident
             ob = wo.logit_bytes
             others[wo.name] = {"kernel_us": 1e3 * kms, "kernel_us_spread": spread_us(kto),
                                "kernel_us_warm": 1e3 * kms_warm,
@@ -396,7 +399,7 @@ def main(argv=None):
         oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device, want_entropy=True)
         for _ in range(3):
             so.verify(*di, out=oo)
-        kms, _ = measure_kernel(so, di, oo, 20, flush=flush)
+        kms, _ = measure_kernel(so, di, oo, REPS, flush=flush)
         ob = wo.logit_bytes
         others[wo.name + "+entropy"] = {"kernel_us": 1e3 * kms, "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
                                         "gbps": ob / (kms / 1e3) / 1e9, "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
@@ -406,7 +409,7 @@ def main(argv=None):
         for _ in range(3):
             so.verify_tv(di[0], di[1], di[3], out=otv)
         so.kernel_times()
-        for _ in range(20):
+        for _ in range(REPS):
             flush.zero_()
             so.verify_tv(di[0], di[1], di[3], out=otv)
         torch.cuda.synchronize()
@@ -427,7 +430,7 @@ def main(argv=None):
         oo = so.alloc_outputs(wo.batch, want_pq=True, want_tv=True, device=device)
         for _ in range(3):
             so.verify(*di, out=oo)
-        kms, kto = measure_kernel(so, di, oo, 20, flush=flush)
+        kms, kto = measure_kernel(so, di, oo, REPS, flush=flush)
         ob = wo.logit_bytes
         others[wo.name] = {"kernel_us": 1e3 * kms, "kernel_us_spread": spread_us(kto),
                            "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3), "gbps": ob / (kms / 1e3) / 1e9,
@@ -445,14 +448,14 @@ def main(argv=None):
                 so.verify_lazy(*di, out=ol)
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             tot = 0.0
-            for _ in range(20):
+            for _ in range(REPS):
                 flush.zero_()
                 ev0.record()
                 so.verify_lazy(*di, out=ol)
                 ev1.record()
                 torch.cuda.synchronize()
                 tot += ev0.elapsed_time(ev1)
-            ms = tot / 20
+            ms = tot / REPS
             tau = np.maximum(ol["tau"].cpu().numpy().astype(np.int64), 0)
             rows = np.where(tau < wo.k, 2 * (tau + 1), 2 * wo.k + 1)
             lb = int(rows.sum()) * wo.vocab * (2 if wo.dtype == si.BF16 else 4)
@@ -475,7 +478,7 @@ def main(argv=None):
             so.loss_grad(di[0], di[1], di[3], kind="overlap", out=og)
         torch.cuda.synchronize()
         so.kernel_times()
-        for _ in range(20):
+        for _ in range(REPS):
             flush.zero_()
             so.loss_grad(di[0], di[1], di[3], kind="overlap", out=og)
         torch.cuda.synchronize()
