@@ -12,13 +12,14 @@
  *   rejection (position tau+1) one token is drawn from the normalised residual
  *   max(0, p - q); if all k are accepted, a bonus token is drawn from p_{k+1}
  *   (the k+1-th target row that the single verification pass provides:
- *   same page, "The draft model moved inside").  The final draw uses its own
- *   uniform u_{k+1} and the inverse CDF y = min{ j : u * S < C_j }.
- *   tau is the accepted length (page "DSpark for GLM-5.2", introduction).
- *   The per-position total-variation distance 0.5 * sum_j |p_i(j) - q_i(j)|
- *   (first page, same section, second bullet) is reported for every
+ *   "Optimizing speculative decoding", section "The draft model moved
+ *   inside").  The final draw uses its own uniform u_{k+1} and the inverse
+ *   CDF y = min{ j : u * S < C_j }.  tau is the accepted length (page
+ *   "DSpark for GLM-5.2", introduction).  The per-position total-variation
+ *   distance 0.5 * sum_j |p_i(j) - q_i(j)| ("Optimizing speculative
+ *   decoding", the section above, second bullet) is reported for every
  *   position; 1 - TV is the per-position acceptance probability
- *   sum_j min(p, q) (first page, section "Kimi K3").
+ *   sum_j min(p, q) ("Optimizing speculative decoding", section "Kimi K3").
  *   T_b == 0 means greedy: p and q are one-hot on the lowest-index maximum,
  *   so a draft is accepted iff it equals the target argmax.
  *
