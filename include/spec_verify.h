@@ -74,7 +74,9 @@ enum { SV_FP32 = 0, SV_BF16 = 1 };
 
 /* Flags for spec_verify_init. */
 enum {
-  SV_FLAG_HOST_STAGING = 1u,  /* also allocate device staging for spec_verify_host */
+  SV_FLAG_HOST_STAGING = 1u,  /* also allocate device staging for spec_verify_host: max_batch
+                                 chains of logits (used only for pageable host logits) and the
+                                 small inputs and outputs */
   SV_FLAG_NO_TMA = 2u,        /* load logits with plain loads instead of bulk copies (testing) */
   SV_FLAG_KERNEL_TIMING = 4u  /* record a CUDA event pair around the verification kernel of each call */
 };
