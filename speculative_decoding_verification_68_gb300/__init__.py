@@ -48,6 +48,71 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# ---------------------------------------------------------------- argument checks
+# The library sees raw pointers and cannot tell a buffer's size, so every
+# tensor is checked here, before the call: a wrong shape would otherwise make
+# the kernels read or write past the end of a buffer.  These raise ValueError
+# (not assert, which python -O removes).
+
+def _check_tensor(t, name: str, dtype, shape: tuple, device):
+    """t must have this dtype and shape, be contiguous, and live on `device`
+    (a torch.device; for CUDA, the same index)."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device.type != device.type or (device.type == "cuda" and t.device.index != device.index):
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def check_batch(k: int, vocab: int, logit_dtype, max_batch: int, device, target, draft, tokens=None,
+                temperature=None, uniforms=None, need_tokens: bool = True, need_uniforms: bool = True) -> int:
+    """Checks a batch of inputs against a handle's k, vocabulary, dtype and
+    capacity; returns the batch size B."""
+    import torch
+    if target is None or target.dim() != 3:
+        raise ValueError("target must be a [B, k+1, V] tensor")
+    B = int(target.shape[0])
+    if B > max_batch:
+        raise ValueError(f"batch {B} exceeds the handle's max_batch {max_batch}")
+    _check_tensor(target, "target", logit_dtype, (B, k + 1, vocab), device)
+    _check_tensor(draft, "draft", logit_dtype, (B, k, vocab), device)
+    if need_tokens:
+        _check_tensor(tokens, "tokens", torch.int32, (B, k), device)
+    _check_tensor(temperature, "temperature", torch.float32, (B,), device)
+    if need_uniforms:
+        _check_tensor(uniforms, "uniforms", torch.float32, (B, k + 1), device)
+    return B
+
+
+def output_shapes(B: int, k: int, vocab: int, logit_dtype) -> dict:
+    """dtype and shape of every output tensor an entry point may write."""
+    import torch
+    f32, i32 = torch.float32, torch.int32
+    return {"tokens": (i32, (B, k + 1)), "tau": (i32, (B,)), "p_draft": (f32, (B, k)), "q_draft": (f32, (B, k)),
+            "tv": (f32, (B, k)), "entropy_target": (f32, (B, k + 1)), "entropy_draft": (f32, (B, k)),
+            "loss": (f32, (B, k)), "grad": (logit_dtype, (B, k, vocab))}
+
+
+def check_outputs(out: dict, B: int, k: int, vocab: int, logit_dtype, device, required=("tokens", "tau")):
+    """Checks the output tensors present in `out` (and that `required` are)."""
+    shapes = output_shapes(B, k, vocab, logit_dtype)
+    for name in required:
+        if out.get(name) is None:
+            raise ValueError(f"output {name} is required")
+    for name, t in out.items():
+        if t is None:
+            continue
+        if name not in shapes:
+            raise ValueError(f"unknown output {name}")
+        dtype, shape = shapes[name]
+        _check_tensor(t, f"output {name}", dtype, shape, device)
+
+
 class SpecVerifier:
     """One library handle: chains of k drafts over a vocabulary of `vocab` tokens."""
 
@@ -60,6 +125,8 @@ class SpecVerifier:
         _check(self._lib.spec_verify_init(ctypes.byref(h), max_batch, k, vocab, self.dtype_code, flags),
                "spec_verify_init")
         self._h = h
+        import torch
+        self.device = torch.device("cuda", torch.cuda.current_device())   # the handle's GPU
 
     @property
     def torch_dtype(self):
@@ -106,19 +173,12 @@ class SpecVerifier:
             out["entropy_draft"] = torch.empty((batch, k), dtype=torch.float32, device=device)
         return out
 
-    def _check_inputs(self, target, draft, tokens, temperature, uniforms):
-        import torch
-        B = target.shape[0]
-        k, V = self.k, self.vocab
-        assert target.dtype == self.torch_dtype and draft.dtype == self.torch_dtype, "logit dtype mismatch"
-        assert tuple(target.shape) == (B, k + 1, V) and tuple(draft.shape) == (B, k, V), "logit shape mismatch"
-        assert target.is_contiguous() and draft.is_contiguous()
-        if tokens is not None:
-            assert tokens.dtype == torch.int32 and tuple(tokens.shape) == (B, k) and tokens.is_contiguous()
-        assert temperature.dtype == torch.float32 and tuple(temperature.shape) == (B,)
-        if uniforms is not None:
-            assert uniforms.dtype == torch.float32 and tuple(uniforms.shape) == (B, k + 1) and uniforms.is_contiguous()
-        return B
+    def _check_inputs(self, target, draft, tokens, temperature, uniforms, device=None, sampling: bool = True):
+        return check_batch(self.k, self.vocab, self.torch_dtype, self.max_batch, device or self.device, target, draft,
+                           tokens, temperature, uniforms, need_tokens=sampling, need_uniforms=sampling)
+
+    def _check_outputs(self, out, B, device=None, required=("tokens", "tau")):
+        check_outputs(out, B, self.k, self.vocab, self.torch_dtype, device or self.device, required)
 
     def verify(self, target, draft, tokens, temperature, uniforms, want_pq: bool = True, want_tv: bool = False,
                out: dict | None = None, stream=None, want_entropy: bool = False) -> dict:
@@ -128,6 +188,9 @@ class SpecVerifier:
         B = self._check_inputs(target, draft, tokens, temperature, uniforms)
         if out is None:
             out = self.alloc_outputs(B, want_pq, want_tv, device=target.device, want_entropy=want_entropy)
+        self._check_outputs(out, B)
+        if (out.get("entropy_target") is None) != (out.get("entropy_draft") is None):
+            raise ValueError("entropy_target and entropy_draft go together")
         args = (self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature), _ptr(uniforms),
                 _ptr(out["tokens"]), _ptr(out["tau"]), _ptr(out.get("p_draft")), _ptr(out.get("q_draft")),
                 _ptr(out.get("tv")))
@@ -146,6 +209,7 @@ class SpecVerifier:
         B = self._check_inputs(target, draft, tokens, temperature, uniforms)
         if out is None:
             out = self.alloc_outputs(B, want_pq=False, want_tv=False, device=target.device)
+        self._check_outputs(out, B)
         rc = self._lib.spec_verify_lazy(self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature),
                                         _ptr(uniforms), _ptr(out["tokens"]), _ptr(out["tau"]), self._stream(stream))
         _check(rc, "spec_verify_lazy")
@@ -157,13 +221,16 @@ class SpecVerifier:
         -ln alpha, alpha = sum min(p, q)) [B, k] fp32 and the gradient of the weighted
         loss with respect to the draft logits [B, k, V] in the logit dtype."""
         import torch
-        B = self._check_inputs(target, draft, None, temperature, None)
+        B = self._check_inputs(target, draft, None, temperature, None, sampling=False)
+        if kind not in ("tv", "overlap"):
+            raise ValueError(f"kind must be 'tv' or 'overlap', not {kind!r}")
         code = {"tv": SV_LOSS_TV, "overlap": SV_LOSS_OVERLAP}[kind]
         if weights is not None:
-            assert weights.dtype == torch.float32 and tuple(weights.shape) == (B, self.k) and weights.is_contiguous()
+            _check_tensor(weights, "weights", torch.float32, (B, self.k), self.device)
         if out is None:
             out = {"loss": torch.empty((B, self.k), dtype=torch.float32, device=target.device),
                    "grad": torch.empty_like(draft)}
+        self._check_outputs(out, B, required=("grad",))
         rc = self._lib.spec_verify_loss_grad(self._h, B, _ptr(target), _ptr(draft), _ptr(temperature), code,
                                              _ptr(weights), _ptr(out.get("loss")), _ptr(out["grad"]),
                                              self._stream(stream))
@@ -173,9 +240,10 @@ class SpecVerifier:
     def verify_tv(self, target, draft, temperature, out=None, stream=None):
         """Per-position TV distance only ([B, k] fp32)."""
         import torch
-        B = self._check_inputs(target, draft, None, temperature, None)
+        B = self._check_inputs(target, draft, None, temperature, None, sampling=False)
         if out is None:
             out = torch.empty((B, self.k), dtype=torch.float32, device=target.device)
+        _check_tensor(out, "out", torch.float32, (B, self.k), self.device)
         rc = self._lib.spec_verify_tv(self._h, B, _ptr(target), _ptr(draft), _ptr(temperature), _ptr(out),
                                       self._stream(stream))
         _check(rc, "spec_verify_tv")
@@ -186,7 +254,10 @@ class SpecVerifier:
         SV_FLAG_HOST_STAGING.  Pinned logits are read in place by the kernels,
         pageable ones copied to the device first.  Synchronise the stream
         before reading out."""
-        B = self._check_inputs(target, draft, tokens, temperature, uniforms)
+        import torch
+        cpu = torch.device("cpu")
+        B = self._check_inputs(target, draft, tokens, temperature, uniforms, device=cpu)
+        self._check_outputs(out, B, device=cpu)
         rc = self._lib.spec_verify_host(self._h, B, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(temperature),
                                         _ptr(uniforms), _ptr(out["tokens"]), _ptr(out["tau"]),
                                         _ptr(out.get("p_draft")), _ptr(out.get("q_draft")), _ptr(out.get("tv")),
@@ -215,5 +286,5 @@ class SpecVerifier:
         return rc, n.value
 
 
-__all__ = ["SpecVerifier", "SpecVerifyError", "build", "SV_FP32", "SV_BF16", "SV_FLAG_HOST_STAGING",
+__all__ = ["SpecVerifier", "SpecVerifyError", "build", "check_batch", "check_outputs", "output_shapes", "SV_FP32", "SV_BF16", "SV_FLAG_HOST_STAGING",
            "SV_FLAG_NO_TMA", "SV_FLAG_KERNEL_TIMING", "SV_OK", "SV_ERR_DATA", "SV_ERR_ARG", "SV_ERR_TIMEOUT"]
