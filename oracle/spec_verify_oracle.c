@@ -28,7 +28,7 @@
  *     completion under which the target distribution is preserved and the
  *     acceptance equals sum min(p, q), and are taken in that reading.
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *   - temperature: p = softmax(z / T) for the target and q = softmax(z / T) for
  *     the draft, the chain's T for both; T == 0 means greedy: the one-hot
  *     distribution on the lowest-index maximum.
