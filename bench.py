@@ -390,6 +390,7 @@ def main(argv=None):
                                "draft_tokens_per_s": wo.batch * wo.k / (kms / 1e3),
                                "chains_per_s": wo.batch / (kms / 1e3), "gbps": ob / (kms / 1e3) / 1e9,
                                "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
+                               "accepted_tokens_per_s": float((oo["tau"].clamp(min=-1) + 1).sum().item()) / (kms / 1e3),
                                "mean_tau": float(oo["tau"].float().mean().item())}
             so.close()
             del di, oo
@@ -464,6 +465,7 @@ def main(argv=None):
             lb = int(rows.sum()) * wo.vocab * (2 if wo.dtype == si.BF16 else 4)
             others[wo.name + "+lazy"] = {"call_us": 1e3 * ms, "draft_tokens_per_s": wo.batch * wo.k / (ms / 1e3),
                                          "chains_per_s": wo.batch / (ms / 1e3), "mean_tau": float(tau.mean()),
+                                         "accepted_tokens_per_s": float((tau + 1).sum()) / (ms / 1e3),
                                          "bytes_read": lb, "gbps": lb / (ms / 1e3) / 1e9,
                                          "frac_of_peak": lb / (ms / 1e3) / 1e9 / peak,
                                          "launches_per_call": 2,
