@@ -382,7 +382,53 @@ def pin_overlap_gradient_finite_differences(orc):
             assert np.allclose(g3, 3.0 * g, rtol=1e-14, atol=0)
 
 
-ALL_PINS = [pin_worked_examples, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
+def pin_tie_band(orc):
+    """The tie flags mark exactly the decisions within 1e-6 of their threshold:
+    an accept test with |u - p(x)/q(x)| < 1e-6, and a final draw with u*S within
+    1e-6*S of the chosen CDF boundary or the one below it.  The thresholds are
+    computed here from scipy's softmax and numpy's cumulative sum.  Greedy
+    decisions are never flagged."""
+    import scipy.special
+    zt = np.array([0.3, -1.0, 0.8, 0.1, -0.4, 0.0], np.float32)   # target row 0
+    zd = np.array([0.9, -0.2, 0.1, 0.4, -0.4, 0.0], np.float32)   # draft row 0
+    zb = np.array([0.5, 0.2, -0.3, 1.1, 0.0, -2.0], np.float32)   # bonus row
+    T = np.float32(1.0)
+    p = scipy.special.softmax(zt.astype(np.float64))
+    q = scipy.special.softmax(zd.astype(np.float64))
+    ratio = p[0] / q[0]
+    assert ratio < 0.9
+    w = np.maximum(p - q, 0.0)
+    C = np.cumsum(w)
+    S = C[-1]
+
+    def run(u0, u1, temp=T):
+        target = np.stack([zt, zb])[None]
+        out = orc.verify(target, zd[None, None], np.array([[0]], np.int32), np.array([temp], np.float32),
+                         np.array([[u0, u1]], np.float32), 0)
+        return out
+
+    # accept tests: flagged inside the band, not outside; the decision itself follows u < ratio
+    for d, flagged in ((-3e-7, True), (3e-7, True), (-5e-6, False), (5e-6, False)):
+        out = run(np.float32(ratio + d), np.float32(0.5))
+        assert bool(out["accept_tie"][0, 0]) == flagged, (d, out["accept_tie"])
+        assert (out["tau"][0] == 1) == (np.float32(ratio + d) < ratio)
+    # final draws after a rejection: u1 close to each inner boundary C_j / S
+    for j in range(len(C) - 1):
+        if w[j] == 0.0 or w[j + 1:].sum() == 0.0:
+            continue
+        for d, flagged in ((-3e-7, True), (3e-7, True), (-5e-6, False), (5e-6, False)):
+            u1 = np.float32(C[j] / S + d)
+            out = run(np.float32(0.999), u1)
+            assert out["tau"][0] == 0
+            assert bool(out["cdf_tie"][0]) == flagged, (j, d, out["cdf_tie"])
+            want = int(np.searchsorted(C, float(u1) * S, side="right"))
+            assert out["tokens"][0, 0] == want
+    # greedy: exact decisions, never flagged
+    out = run(np.float32(ratio), np.float32(C[0] / S), temp=np.float32(0.0))
+    assert out["accept_tie"][0, 0] == 0 and out["cdf_tie"][0] == 0
+
+
+ALL_PINS = [pin_worked_examples, pin_tie_band, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
             pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact,
             pin_entropy_closed_forms, pin_entropy_library, pin_overlap_loss_values,
             pin_overlap_gradient_finite_differences]

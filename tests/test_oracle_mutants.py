@@ -35,6 +35,10 @@ MUTANTS = {
                                "grad[j] = w * dl * (qj / T) * ((qj > pj ? 1.0 : 0.0) - beta);"),
     "grad_beta_dropped": ("grad[j] = w * dl * (qj / T) * ((qj < pj ? 1.0 : 0.0) - beta);",
                           "grad[j] = w * dl * (qj / T) * (qj < pj ? 1.0 : 0.0);"),
+    "tie_band_too_wide": ("#define SO_TIE_BAND 1e-6", "#define SO_TIE_BAND 1e-4"),
+    "cdf_tie_below_boundary_missed": (
+        "if (tie) *tie = fabs(t - C) < SO_TIE_BAND * S || fabs(t - Cprev) < SO_TIE_BAND * S;",
+        "if (tie) *tie = fabs(t - C) < SO_TIE_BAND * S;"),
     "overlap_loss_log_missing": ("*loss = kind == 0 ? 1.0 - alpha : -log(alpha);", "*loss = kind == 0 ? 1.0 - alpha : -alpha;"),
 }
 
