@@ -428,7 +428,93 @@ def pin_tie_band(orc):
     assert out["accept_tie"][0, 0] == 0 and out["cdf_tie"][0] == 0
 
 
+def _padded_rows(rng, rows, pad, V, scale, dtype):
+    """[rows, V] logits that are the head of a larger buffer with `pad` extra
+    random rows behind them, so that a batch driver that mis-strides a row
+    still reads inside the allocation (the pins then see wrong values, not a
+    crash).  fp32 or bf16 storage (bf16: the high half of the fp32 bits)."""
+    z = (rng.standard_normal((rows + pad, V)) * scale).astype(np.float32)
+    if dtype == si.BF16:
+        z = (z.view(np.uint32) >> 16).astype(np.uint16)
+    return z, z[:rows]
+
+
+def _row_values(z, dtype):
+    """fp64 logit values of stored rows (bf16 bits widened exactly)."""
+    if dtype == si.BF16:
+        return (z.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return z.astype(np.float64)
+
+
+def pin_batch_drivers(orc):
+    """The batch drivers of the entropy and the overlap losses map chain b,
+    position i to target row b*(k+1)+i, draft row b*k+i, the chain's
+    temperature T[b] and the weight w[b, i].  Checked per row against scipy's
+    softmax / entropy (independent of the oracle), against the single-row
+    functions on explicitly indexed rows (bit-equal), and, for the weights,
+    by the gradient's linearity in w[b, i] (page "Optimizing speculative
+    decoding", sections "Kimi K3" and "Rejection sampling and a loss that
+    optimizes acceptance directly")."""
+    import scipy.special
+    import scipy.stats
+    rng = np.random.default_rng(41)
+    B, k, V = 4, 3, 24
+    T = np.array([0.7, 0.0, 1.3, 1.0], np.float32)        # chain 1 greedy
+    w = rng.uniform(0.5, 2.0, (B, k)).astype(np.float32)   # distinct weights per (b, i)
+    for dtype in (si.FP32, si.BF16):
+        big_t, t2 = _padded_rows(rng, B * (k + 1), B * (k + 1), V, 2.0, dtype)
+        big_d, d2 = _padded_rows(rng, B * k, B * (k + 1), V, 2.0, dtype)
+        nan_bits = np.float32(np.nan).view(np.uint32) >> 16 if dtype == si.BF16 else np.float32(np.nan)
+        t2[3 * (k + 1) + 1, 5] = nan_bits                  # chain 3: target row 1 is invalid
+        target, draft = t2.reshape(B, k + 1, V), d2.reshape(B, k, V)
+        tv, dv = _row_values(target, dtype), _row_values(draft, dtype)
+
+        # ---- entropies
+        ent_t, ent_d = orc.entropy_batch(target, draft, T, dtype)
+        assert ent_t.shape == (B, k + 1) and ent_d.shape == (B, k)
+        for b in range(B):
+            for rows, vals, ent in ((target, tv, ent_t), (draft, dv, ent_d)):
+                for i in range(rows.shape[1]):
+                    one = orc.entropy(rows[b, i], float(T[b]), dtype=dtype)
+                    got = ent[b, i]
+                    assert (math.isnan(one) and math.isnan(got)) or one == got, (dtype, b, i, got, one)
+                    if np.isnan(vals[b, i]).any():
+                        assert math.isnan(got), (b, i)
+                    elif T[b] == 0:
+                        assert got == 0.0
+                    else:
+                        want = scipy.stats.entropy(scipy.special.softmax(vals[b, i] / float(T[b])))
+                        assert abs(got - want) <= 1e-11 * max(1.0, want), (dtype, b, i, got, want)
+
+        # ---- losses, overlaps and gradients
+        for kind in (0, 1):
+            r = orc.overlap_grad_batch(target, draft, T, kind, w, dtype)
+            r1 = orc.overlap_grad_batch(target, draft, T, kind, None, dtype)
+            for b in range(B):
+                for i in range(k):
+                    loss, alpha, g, tie = orc.overlap_grad(target[b, i], draft[b, i], float(T[b]), kind,
+                                                           float(w[b, i]), dtype=dtype)
+                    for name, one in (("loss", loss), ("alpha", alpha), ("tie", tie)):
+                        got = r[name][b, i]
+                        assert (math.isnan(one) and math.isnan(got)) or one == got, (name, dtype, kind, b, i)
+                    assert np.array_equal(r["grad"][b, i], g), (dtype, kind, b, i)
+                    invalid = T[b] <= 0 or np.isnan(tv[b, i]).any()
+                    if invalid:
+                        assert math.isnan(r["loss"][b, i]) and not np.any(r["grad"][b, i])
+                        continue
+                    p = scipy.special.softmax(tv[b, i] / float(T[b]))
+                    q = scipy.special.softmax(dv[b, i] / float(T[b]))
+                    a = float(np.minimum(p, q).sum())
+                    assert abs(r["alpha"][b, i] - a) <= 1e-12, (dtype, kind, b, i)
+                    want = 1.0 - a if kind == 0 else -math.log(a)
+                    assert abs(r["loss"][b, i] - want) <= 1e-12 * max(1.0, abs(want))
+                    # the weight enters the gradient linearly, and only its own position's
+                    g1 = r1["grad"][b, i] * float(w[b, i])
+                    assert np.allclose(r["grad"][b, i], g1, rtol=1e-14, atol=1e-300), (dtype, kind, b, i)
+                    assert np.any(r["grad"][b, i])
+
+
 ALL_PINS = [pin_worked_examples, pin_tie_band, pin_inverse_cdf_library, pin_softmax_library, pin_argmax_library, pin_tv_identities,
             pin_acceptance_is_overlap, pin_greedy_is_argmax_match, pin_target_preservation_exact,
             pin_entropy_closed_forms, pin_entropy_library, pin_overlap_loss_values,
-            pin_overlap_gradient_finite_differences]
+            pin_overlap_gradient_finite_differences, pin_batch_drivers]

@@ -40,6 +40,16 @@ MUTANTS = {
         "if (tie) *tie = fabs(t - C) < SO_TIE_BAND * S || fabs(t - Cprev) < SO_TIE_BAND * S;",
         "if (tie) *tie = fabs(t - C) < SO_TIE_BAND * S;"),
     "overlap_loss_log_missing": ("*loss = kind == 0 ? 1.0 - alpha : -log(alpha);", "*loss = kind == 0 ? 1.0 - alpha : -alpha;"),
+    # batch drivers: row strides, the draft row's buffer, and the weight index
+    "entropy_target_row_stride": ("so_entropy((const char*)J->target + (size_t)(b * (J->k + 1) + i) * rs",
+                                  "so_entropy((const char*)J->target + (size_t)(b * J->k + i) * rs"),
+    "entropy_draft_row_from_target": ("so_entropy((const char*)J->draft + (size_t)(b * J->k + (i - J->k - 1)) * rs",
+                                      "so_entropy((const char*)J->target + (size_t)(b * J->k + (i - J->k - 1)) * rs"),
+    "grad_target_row_stride": ("so_overlap_grad((const char*)J->target + (size_t)(b * (J->k + 1) + i) * rs",
+                               "so_overlap_grad((const char*)J->target + (size_t)(b * J->k + i) * rs"),
+    "grad_draft_row_stride": ("(const char*)J->draft + (size_t)(b * J->k + i) * rs, J->dtype",
+                              "(const char*)J->draft + (size_t)(b * (J->k + 1) + i) * rs, J->dtype"),
+    "grad_weight_per_chain": ("J->w ? (double)J->w[r] : 1.0", "J->w ? (double)J->w[b] : 1.0"),
 }
 
 
