@@ -133,6 +133,31 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+def workload_config(w: si.Workload, nb: int, world: int) -> dict:
+    """The `config` object of the JSON line, identical for both arms."""
+    es = 2 if w.dtype == si.BF16 else 4
+    return {"workload": w.name, "batch_per_gpu": nb, "global_batch": nb * world, "k": w.k, "vocab": w.vocab,
+            "logit_dtype": "bf16" if w.dtype == si.BF16 else "fp32", "tv_output": bool(w.want_tv),
+            "l2": f"inputs larger than L2 ({nb * (2 * w.k + 1) * w.vocab * es / 1e9:.2f} GB of logits per step per GPU)",
+            "parallelism": f"replicas x{world} (chains sharded, no collective)"}
+
+
+def oracle_parity(b: si.Batch, got: dict) -> dict:
+    """The GPU's outputs for batch b against the CPU oracle on the same inputs:
+    chains compared, exact, decisions the oracle flagged within 1e-6 of their
+    threshold (ties_flagged), chains that differ at such a tie (tie_mismatch),
+    chains that differ elsewhere (beyond_band, must be 0) and the largest
+    errors of p(x), q(x) and TV.  Runs outside every timed region."""
+    import oracle
+    from oracle import parity
+    w = b.workload
+    ref = oracle.default().verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype,
+                                  want_tv="tv" in got, nthreads=os.cpu_count() or 1)
+    res = parity.compare({k: v.cpu().numpy() if hasattr(v, "cpu") else v for k, v in got.items()}, ref)
+    res.pop("first_beyond_band", None) if res["ok"] else None
+    return res
+
+
 def device_batch(b: si.Batch, device):
     import torch
     if b.workload.dtype == si.BF16:
@@ -201,10 +226,9 @@ def reference_arm(args, w: si.Workload, rank: int):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "k": w.k, "vocab": w.vocab,
-                       "logit_dtype": "bf16" if w.dtype == si.BF16 else "fp32", "sample_chains_per_step": nb},
+            "config": workload_config(w, w.batch, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{nb} of {w.batch} chains per step"},
+                             "sample": f"{nb} of {w.batch} chains of {w.name} per step (fp64 C oracle, {cores} threads)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -372,9 +396,10 @@ def main(argv=None):
 
     # ---- the other 151,552-vocabulary workloads (kernel time, L2 flushed between calls)
     others = {}
+    check = rank == 0 and world == 1 and not args.no_cpu_baseline   # the CPU leg: oracle parity counts
     if not args.no_others and rank == 0:
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
-        for wo in (si.C3_T0, si.C3_T06, si.C3_T1, si.C4, si.C2):
+        for wo in (si.TINY, si.C2, si.C3_T0, si.C3_T06, si.C3_T1, si.C4):
             bo = si.generate(wo)
             di = device_batch(bo, device)
             so = svlib.SpecVerifier(wo.batch, wo.k, wo.vocab, "bf16" if wo.dtype == si.BF16 else "fp32",
@@ -392,6 +417,8 @@ def main(argv=None):
                                "frac_of_peak": ob / (kms / 1e3) / 1e9 / peak,
                                "accepted_tokens_per_s": float((oo["tau"].clamp(min=-1) + 1).sum().item()) / (kms / 1e3),
                                "mean_tau": float(oo["tau"].float().mean().item())}
+            if check:
+                others[wo.name]["parity"] = oracle_parity(bo, oo)
             so.close()
             del di, oo
         # the main workload again through spec_verify_ex: verification plus the entropy of every row
@@ -498,7 +525,9 @@ def main(argv=None):
         del flush
 
     cpu = None
+    parity_main = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        parity_main = oracle_parity(batch, out)   # the last timed step's outputs, every chain
         cpu = cpu_baseline(w0)
 
     if rank == 0:
@@ -507,11 +536,8 @@ def main(argv=None):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == si.BF16 else "fp32", "data": "synthetic",
-            "config": {"workload": w0.name, "batch_per_gpu": nb, "global_batch": chains_total, "k": w.k,
-                       "vocab": w.vocab, "logit_dtype": dt_name, "tv_output": bool(w.want_tv),
-                       "l2": f"inputs larger than L2 ({alg_bytes / 1e9:.2f} GB of logits per step per GPU)",
-                       "parallelism": f"replicas x{world} (chains sharded, no collective)",
-                       "launch": info},
+            "config": workload_config(w0, nb, world),
+            "launch": info,
             "chains_per_s": chains_total / (ms_step / 1e3),
             "accepted_tokens_per_s": float((tau + 1).sum()) * world / (ms_step / 1e3),
             "hbm_gbps": alg_bytes * world / (ms_step / 1e3) / 1e9 / world,
@@ -531,6 +557,8 @@ def main(argv=None):
             line["e2e"] = e2e
         if cpu:
             line["cpu_baseline"] = cpu
+        if parity_main:
+            line["parity"] = parity_main
         print(json.dumps(line), flush=True)
     sv.close()
     if world > 1:

@@ -66,7 +66,8 @@ enum {
   SV_ERR_CUDA = 4,    /* a CUDA runtime call or launch failed */
   SV_ERR_ALLOC = 5,   /* device or host allocation failed in init */
   SV_ERR_DATA = 6,    /* (get_error) some chains were invalid since the last check */
-  SV_ERR_TIMEOUT = 7  /* (get_error) a bounded device wait expired; outputs of that call are unreliable */
+  SV_ERR_TIMEOUT = 7  /* (get_error) a bounded device wait expired: from then until get_error clears
+                         the flag, every call reports every chain invalid (tau = -1, TV NaN) */
 };
 
 /* Logit element types. */
@@ -199,8 +200,9 @@ int spec_verify_ex(spec_verify_t h, int batch,
  * calls share the one array and its contents persist between calls (the
  * counters that must start at zero are cleared on the stream at each call),
  * so calls that overlap on the GPU, on different streams, race with each
- * other: order them on one stream.  Data and timeout counters of this call
- * are not reported; invalid chains show up as tau = -1. */
+ * other: order them on one stream.  Counters are not reported: invalid
+ * chains show up as tau = -1, and a bounded device wait that gives up during
+ * a call makes that call report every chain invalid (tau = -1, TV NaN). */
 #define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
 int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype,
                         const void* target_logits, const void* draft_logits,
@@ -246,8 +248,10 @@ int spec_verify_get_error(spec_verify_t h, int* invalid_count);
  * timeout flag; the second must then see the flag and return early.  Nothing
  * is left in flight, so the context stays usable.  Synchronises, stores the
  * SM clock cycles each wait took in elapsed_cycles[0..1] (nullable), and
- * returns what spec_verify_get_error returns: SV_ERR_TIMEOUT when the waits
- * expired as they should.  SV_ERR_ARG for polls < 1. */
+ * returns the handle's status without clearing it: SV_ERR_TIMEOUT when the
+ * waits expired as they should.  The flag then stays set, as after a real
+ * timeout, so calls on the handle report every chain invalid until
+ * spec_verify_get_error clears it.  SV_ERR_ARG for polls < 1. */
 int spec_verify_selftest_wait(spec_verify_t h, int polls, long long* elapsed_cycles);
 
 /* Launch geometry chosen at init: vocabulary slices per row (thread-block

@@ -96,7 +96,7 @@ struct KParams {
   float* ws_p;               // [B, k+1, items] share of sum e_t per warp range
   int* flags;                // [0] invalid count, [1] wait timeout
   int B, k, V, Vs;
-  int wv;                    // vectors per warp: ceil(ceil(Vs / EPV) / NWARP)
+  int rbase, rextra;         // rounds of 32 vectors per warp: rbase, one more for the last rextra warps
   int units_per_chain;       // k+1 (verify) or k (TV only)
   int tv_only;
   int tma;                   // bulk copies into the stage
@@ -274,13 +274,19 @@ template <> struct Lay<__nv_bfloat16> {
 // Unscaled residual weights of one pair of elements: max(0, e_t - r * e_d)
 // with e = 2^(z*c - R) and r = S_t / S_d, i.e. S_t * max(0, p - q).  One
 // rounding after an exact product, so identical rows give exactly zero.
-__device__ __forceinline__ u64 pair_w(float t0, float t1, float d0, float d1, u64 cc, u64 nrt, u64 nrd, u64 nr) {
+// The clamp is the fma's saturation to [0, 1], which is exact here: the row
+// reference R is at least the row maximum times c, so e_t <= 1 and
+// e_t - r * e_d <= 1.  (The packed fma has no saturating form.)
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ u64 pair_w(float t0, float t1, float d0, float d1, u64 cc, u64 nrt, u64 nrd, float nr) {
   float at0, at1, ad0, ad1;
   upk(fma2(pk(t0, t1), cc, nrt), at0, at1);
   upk(fma2(pk(d0, d1), cc, nrd), ad0, ad1);
-  float w0, w1;
-  upk(fma2(pk(ex2(ad0), ex2(ad1)), nr, pk(ex2(at0), ex2(at1))), w0, w1);
-  return pk(fmaxf(w0, 0.0f), fmaxf(w1, 0.0f));
+  return pk(fma_sat(ex2(ad0), nr, ex2(at0)), fma_sat(ex2(ad1), nr, ex2(at1)));
 }
 // Unscaled target weights of one pair of elements: e_t = S_t * p.
 __device__ __forceinline__ u64 pair_p(float t0, float t1, u64 cc, u64 nrt) {
@@ -291,7 +297,7 @@ __device__ __forceinline__ u64 pair_p(float t0, float t1, u64 cc, u64 nrt) {
 
 // Sum of the weights of one vector (residual if PAIR, else target).
 template <typename Tl, bool PAIR>
-__device__ __forceinline__ float vec_weight_sum(const uint4& t, const uint4& d, u64 cc, u64 nrt, u64 nrd, u64 nr) {
+__device__ __forceinline__ float vec_weight_sum(const uint4& t, const uint4& d, u64 cc, u64 nrt, u64 nrd, float nr) {
   u64 acc;
   if constexpr (sizeof(Tl) == 4) {
     if (PAIR) acc = add2(pair_w(__uint_as_float(t.x), __uint_as_float(t.y), __uint_as_float(d.x), __uint_as_float(d.y), cc, nrt, nrd, nr),
@@ -314,7 +320,7 @@ __device__ __forceinline__ float vec_weight_sum(const uint4& t, const uint4& d, 
 
 // Individual weights of one vector (same arithmetic as above, element by element).
 template <typename Tl>
-__device__ __forceinline__ void vec_weights(const uint4& t, const uint4& d, bool pair, u64 cc, u64 nrt, u64 nrd, u64 nr,
+__device__ __forceinline__ void vec_weights(const uint4& t, const uint4& d, bool pair, u64 cc, u64 nrt, u64 nrd, float nr,
                                             float (&w)[Lay<Tl>::EPV]) {
   constexpr int EPV = Lay<Tl>::EPV;
 #pragma unroll
@@ -369,12 +375,14 @@ template <> struct MaxAcc<__nv_bfloat16> {
   __device__ __forceinline__ float get() const { return nanmax(__low2float(m), __high2float(m)); }
 };
 
-// Sum of 2^(z*c + nref) over R vectors with independent packed accumulators.
+// Sum of 2^(z*c + nref) over R vectors with independent packed accumulators
+// (the last vector only if `last`: a warp without a last round holds padding there).
 template <typename Tl, int R>
-__device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr) {
+__device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr, bool last) {
   u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     float x0, x1, x2, x3;
     if constexpr (sizeof(Tl) == 4) {
       upk(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr), x0, x1);
@@ -409,11 +417,12 @@ __device__ __forceinline__ u64 clamp_m127(u64 x) {
   return pk(fmaxf(lo, -127.0f), fmaxf(hi, -127.0f));
 }
 template <typename Tl, int R>
-__device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, float& ea) {
+__device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, bool last, float& ea) {
   u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
   u64 m0 = 0ull, m1 = 0ull, m2 = 0ull, m3 = 0ull;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     u64 x0, x1, x2, x3;
     if constexpr (sizeof(Tl) == 4) {
       x0 = clamp_m127(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr));
@@ -451,12 +460,30 @@ __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u6
 __device__ __forceinline__ float row_entropy(float S, float EA) { return logf(S) - LN2_F * (EA / S); }
 
 // ------------------------------------------------------------- fused kernel
-// Vector v of a CTA's slice (16 bytes: EPV logits) belongs to warp v / WV,
-// round (v % WV) / 32, lane v % 32, where WV = ceil(nvec / NWARP): every warp
-// owns a contiguous range of the vocabulary, and (rank, warp) items are in
-// vocabulary order.  In shared memory each warp's range of each row has its
-// own block of R*32 vectors; the tail past the range stays -inf, so the
-// copy into registers needs no bounds checks.
+// A CTA's slice is read in rounds of 32 16-byte vectors (EPV logits each),
+// one vector per lane.  Its ceil(nvec / 32) rounds are split over the NWARP
+// warps as evenly as possible: every warp takes rbase rounds and the last
+// rextra warps one more, so no warp computes a round of padding that a
+// lighter split would avoid (at V = 151,552 bf16: 74 rounds, six warps of 9
+// and two of 10, instead of eight of 10 with 7.5% padding).  Warp w owns the
+// contiguous vectors [warp_vbeg(w), warp_vbeg(w) + 32 * warp_rounds(w)), so
+// (rank, warp) items are in vocabulary order; round j, lane l holds vector
+// warp_vbeg(w) + 32 j + l.  In shared memory each warp's range of each row has
+// its own block of R*32 vectors (R >= every warp's rounds); the tail past
+// the range stays -inf, so the copy into registers needs no bounds checks.
+__host__ __device__ __forceinline__ int warp_rounds(int w, int rbase, int rextra) {
+  return rbase + (w >= NWARP - rextra ? 1 : 0);
+}
+__host__ __device__ __forceinline__ int warp_vbeg(int w, int rbase, int rextra) {
+  const int lo = NWARP - rextra;   // warps with rbase rounds
+  return 32 * (w * rbase + (w > lo ? w - lo : 0));
+}
+// The warp whose range holds vector lv of the slice.
+__device__ __forceinline__ int warp_of_vec(int lv, int rbase, int rextra) {
+  const int ri = lv >> 5, lo = NWARP - rextra;
+  if (ri < lo * rbase) return ri / rbase;
+  return lo + (ri - lo * rbase) / (rbase + 1);
+}
 struct Geo {
   const KParams* p;
   __device__ __forceinline__ unsigned C() const { return cl_size(); }
@@ -464,7 +491,8 @@ struct Geo {
   __device__ __forceinline__ int items() const { return (int)cl_size() * NWARP; }
   __device__ __forceinline__ int slice0() const { return (int)cl_rank() * p->Vs; }
   __device__ __forceinline__ int slen() const { return max(0, min(p->Vs, p->V - slice0())); }
-  __device__ __forceinline__ int vbeg() const { return (int)(threadIdx.x >> 5) * p->wv; }
+  __device__ __forceinline__ int vbeg() const { return warp_vbeg((int)(threadIdx.x >> 5), p->rbase, p->rextra); }
+  __device__ __forceinline__ int rounds() const { return warp_rounds((int)(threadIdx.x >> 5), p->rbase, p->rextra); }
 };
 
 // Units are taken position-major, u = ipos * B + b, so that every cluster's
@@ -503,8 +531,8 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
   __syncwarp();
   const int w = lane & 7, row = lane >> 3;
   if (lane < 16 && (row == 0 || pair)) {
-    const int vb = w * P.wv;
-    const int len = max(0, min(P.wv, nvec_of<Tl>(g) - vb));
+    const int vb = warp_vbeg(w, P.rbase, P.rextra);
+    const int len = max(0, min(32 * warp_rounds(w, P.rbase, P.rextra), nvec_of<Tl>(g) - vb));
     if (len > 0) {
       const char* src = (const char*)(row == 0 ? P.target : P.draft) +
                         ((size_t)(row == 0 ? trow : drow) * P.V + g.slice0()) * ES + (size_t)vb * 16;
@@ -547,17 +575,19 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   // ---------------- this warp's vectors of the unit into registers
   uint4 rt[R], rd[R];
   bool own_x = false;
+  const bool last = g.rounds() == R;   // warp-uniform: this warp owns a last round
   if (P.tma) {
     mbar_wait_bounded(bar, phase, P.flags);
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      rt[j] = blk_t[j * 32 + lane];
-      if (PAIR) rd[j] = blk_d[j * 32 + lane];
+      const bool in = j < R - 1 || last;   // else padding: -inf without a load
+      rt[j] = in ? blk_t[j * 32 + lane] : Lay<Tl>::neg_inf();
+      if (PAIR) rd[j] = in ? blk_d[j * 32 + lane] : Lay<Tl>::neg_inf();
     }
     own_x = !LAZY && PAIR && !P.tv_only && x >= 0 && x < V && (long long)x >= g.slice0() && (long long)x < g.slice0() + g.slen();
     if (PAIR && tid == 0 && own_x) {
       const int lx = (int)(x - g.slice0());
-      const int lv = lx / EPV, wb = lv / P.wv, iv = lv - wb * P.wv;
+      const int lv = lx / EPV, wb = warp_of_vec(lv, P.rbase, P.rextra), iv = lv - warp_vbeg(wb, P.rbase, P.rextra);
       const unsigned char* bt = smem_stage + ((size_t)(0 * NWARP + wb) * R * 32 + iv) * 16;
       const unsigned char* bd = smem_stage + ((size_t)(1 * NWARP + wb) * R * 32 + iv) * 16;
       S.gz_t = Lay<Tl>::load_scalar(bt, lx % EPV);
@@ -575,7 +605,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const int v = g.vbeg() + j * 32 + lane;
-      const bool in = v < min(g.vbeg() + P.wv, nvec_of<Tl>(g));
+      const bool in = j < g.rounds() && v < nvec_of<Tl>(g);
       if (P.vec16) {   // the tail vector of a 16-byte-aligned row is whole (the row length is too)
         rt[j] = in ? __ldg(reinterpret_cast<const uint4*>(tb) + v) : Lay<Tl>::neg_inf();
         if (PAIR) rd[j] = in ? __ldg(reinterpret_cast<const uint4*>(db) + v) : Lay<Tl>::neg_inf();
@@ -606,6 +636,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   MaxAcc<Tl> mx_t, mx_d;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     mx_t.add(rt[j]);
     if (PAIR) mx_d.add(rd[j]);
   }
@@ -634,11 +665,11 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     if constexpr (ENT) {   // the index fields carry sum e*a for sampling units
       float ea_t = 0.0f, ea_d = 0.0f;
-      mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), ea_t);
+      mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), last, ea_t);
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = rows_expsum_ent<Tl, R>(rd, cc, pk(-rwd, -rwd), ea_d);
+        mine.s_d = rows_expsum_ent<Tl, R>(rd, cc, pk(-rwd, -rwd), last, ea_d);
       }
       float v0 = mine.s_t, v1 = mine.s_d, v2 = ea_t, v3 = ea_d;
 #pragma unroll
@@ -651,11 +682,11 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       mine.s_t = v0; mine.s_d = v1;
       mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
     } else {
-      mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
+      mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+        mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd), last));
       }
     }
   }
@@ -803,10 +834,11 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   // ---------------- pass B: residual mass of this warp's range
   const u64 cc = pk(c, c);
   const u64 nrt = pk(-M.R_t, -M.R_t), nrd = pk(-M.R_d, -M.R_d);
-  const u64 nr = pk(-M.r, -M.r);
+  const float nr = -M.r;
   float w0 = 0.0f, w1 = 0.0f;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     const float wj = vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr);
     if (j & 1) w1 += wj; else w0 += wj;
   }
@@ -968,7 +1000,7 @@ struct FParams {
   int32_t* out_tau;
   float* out_tv;
   int* flags;
-  int B, k, V, Vs, wv, items, vec16, tv_only;   // vec16: rows 16-byte aligned
+  int B, k, V, Vs, rbase, rextra, items, vec16, tv_only;   // vec16: rows 16-byte aligned
   int lazy;   // positions after the first rejection were not verified
 };
 
@@ -998,6 +1030,10 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
   }
   const int tok = !F.tv_only && lane < k ? F.tokens[(size_t)b * k + lane] : -1;
   const float u_fin = F.tv_only ? 0.0f : F.uniforms[ub + k];   // the final draw uses u[b, k]
+  // A bounded wait that gave up (in this call, or in an earlier one whose flag
+  // has not been cleared by spec_verify_get_error) leaves the statistics
+  // unreliable: every chain is then reported invalid, and every TV is NaN.
+  const bool timed_out = *(volatile const int*)&F.flags[1] != 0;
 
   const unsigned rej = __ballot_sync(FULL, lane < k && a == 0);
   const int tau = rej ? __ffs(rej) - 1 : k;
@@ -1031,10 +1067,11 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
       v += __shfl_xor_sync(FULL, v, 2);
       if (q == 0 && ok) F.out_tv[(size_t)b * k + i] = v / S_t;
     }
+    if (timed_out && lane < k) F.out_tv[(size_t)b * k + lane] = __int_as_float(0x7fc00000);
   }
-  if (bad && lane == 0) atomicAdd(&F.flags[0], 1);
+  if (bad && !timed_out && lane == 0) atomicAdd(&F.flags[0], 1);
   if (F.tv_only) return;
-  if (bad) {
+  if (bad || timed_out) {
     if (lane <= k) F.out_tokens[ub + lane] = -1;
     if (lane == 0) F.out_tau[b] = -1;
     return;
@@ -1096,7 +1133,8 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
     const long long slice0 = (long long)crank * F.Vs;
     const int slen = (int)max(0LL, min((long long)F.Vs, (long long)F.V - slice0));
     const int nvec = (slen + EPV - 1) / EPV;
-    const int vbeg = cwarp * F.wv, vend = min(vbeg + F.wv, nvec);
+    const int vbeg = warp_vbeg(cwarp, F.rbase, F.rextra);
+    const int vend = min(vbeg + 32 * warp_rounds(cwarp, F.rbase, F.rextra), nvec);
     const bool use_pair = pair && !fallback;
     const char* tb = (const char*)F.target + ((size_t)(ub + tau) * F.V + slice0) * ES;
     const char* db = (const char*)F.draft + (((size_t)b * k + (pair ? tau : 0)) * F.V + slice0) * ES;
@@ -1113,7 +1151,8 @@ __global__ void __launch_bounds__(256) sv_finalize_kernel(const FParams F) {
       }
     }
     const u64 cc = pk(us.c, us.c);
-    const u64 nrt = pk(-us.R_t, -us.R_t), nrd = pk(-us.R_d, -us.R_d), nr = pk(-us.r, -us.r);
+    const u64 nrt = pk(-us.R_t, -us.R_t), nrd = pk(-us.R_d, -us.R_d);
+    const float nr = -us.r;
     float wl[R];
 #pragma unroll
     for (int j = 0; j < R; ++j)
@@ -1253,12 +1292,14 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
 
   uint4 rt[R], rd[R];
+  const bool last = g.rounds() == R;   // warp-uniform: this warp owns a last round
   if (P.tma) {
     mbar_wait_bounded(bar, phase, P.flags);
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      rt[j] = blk_t[j * 32 + lane];
-      rd[j] = blk_d[j * 32 + lane];
+      const bool in = j < R - 1 || last;   // else padding: -inf without a load
+      rt[j] = in ? blk_t[j * 32 + lane] : Lay<Tl>::neg_inf();
+      rd[j] = in ? blk_d[j * 32 + lane] : Lay<Tl>::neg_inf();
     }
     __syncwarp();
     bool last = false;
@@ -1268,7 +1309,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   } else {
     const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0()) * ES;
     const char* db = (const char*)P.draft + ((size_t)drow * V + g.slice0()) * ES;
-    const int nv = nvec_of<Tl>(g), vb = g.vbeg(), ve = min(vb + P.wv, nv);
+    const int nv = nvec_of<Tl>(g), vb = g.vbeg(), ve = min(vb + 32 * g.rounds(), nv);
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const int v = vb + j * 32 + lane;
@@ -1284,6 +1325,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   MaxAcc<Tl> mx_t, mx_d;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     mx_t.add(rt[j]);
     mx_d.add(rd[j]);
   }
@@ -1297,8 +1339,8 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   {
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-    mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt)));
-    mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd)));
+    mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
+    mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd), last));
   }
   const int item = g.rank() * NWARP + warp;
   {
@@ -1349,7 +1391,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   if (M.status != 0) {   // invalid position: zero gradient, NaN loss
 #pragma unroll
     for (int j = 0; j < R; ++j)
-      if (j * 32 + lane < P.wv) store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(0u, 0u, 0u, 0u));
+      if (j < g.rounds()) store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(0u, 0u, 0u, 0u));
     if (tid == 0 && g.rank() == 0 && P.out_loss) P.out_loss[(size_t)b * k + ipos] = __int_as_float(0x7fc00000);
     return;
   }
@@ -1362,6 +1404,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   u64 b1 = 0ull, b2 = 0ull;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
 #pragma unroll
     for (int e = 0; e < EPV; e += 2) {
       const float t0 = Lay<Tl>::elem(rt[j], e), t1 = Lay<Tl>::elem(rt[j], e + 1);
@@ -1427,6 +1470,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
   const float sel1 = G.K * (1.0f - G.beta), sel0 = -G.K * G.beta;
 #pragma unroll
   for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
     uint32_t wd[4];
 #pragma unroll
     for (int e = 0; e < EPV; e += 2) {
@@ -1440,7 +1484,7 @@ __device__ __forceinline__ void grad_unit(const KParams& P, Small& S, GradStat* 
       if constexpr (sizeof(Tl) == 4) { wd[e] = __float_as_uint(g0); wd[e + 1] = __float_as_uint(g1); }
       else wd[e >> 1] = bf16x2_rn(g0, g1);   // rounded to nearest even
     }
-    if (j * 32 + lane < P.wv)
+    if (j < g.rounds())
       store_grad<Tl>(grow, vb + j * 32 + lane, slen, P.grad_vec, make_uint4(wd[0], wd[1], wd[2], wd[3]));
     if (j + 1 < R) {
       u64 dep = pk(__uint_as_float(wd[0]), __uint_as_float(wd[1]));
@@ -1542,7 +1586,7 @@ struct spec_verify_ctx {
   int device;
   int max_batch, k, V, dtype;
   unsigned flags;
-  int C, Vs, R, wv, n_clusters, tma_ok;
+  int C, Vs, R, rbase, rextra, n_clusters, tma_ok;
   size_t smem;
   FusedFn kernel;
   FusedFn kernel_ent;        // the same kernel that also writes row entropies
@@ -1576,6 +1620,19 @@ struct spec_verify_ctx {
 };
 
 static constexpr int TIMING_RING = 4096;
+
+// Dynamic shared memory of one CTA with R register rounds: the bookkeeping
+// area, and the bulk-copy stage (two rows of NWARP blocks of R*32 vectors).
+// Kernels with plain loads use only the bookkeeping area.
+static size_t smem_bytes(int R, bool tma) { return SMALL_BYTES + (tma ? 2 * (size_t)NWARP * R * 32 * 16 : 0); }
+
+// The opt-in limit is a property of the kernel, shared by every handle and
+// plan that launches it: set it to the largest size any launch of this R asks
+// for (the staged one), so that opening a handle with plain loads never
+// lowers it under a live handle that stages.
+static bool set_smem_limit(FusedFn f, int R) {
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(R, true)) == cudaSuccess;
+}
 
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
@@ -1629,7 +1686,7 @@ static int launch_finalize(spec_verify_ctx* h, const KParams& P, const int32_t* 
   F.target = P.target; F.draft = P.draft; F.tokens = tokens; F.uniforms = P.uniforms;
   F.ws_acc = P.ws_acc; F.ws_y = P.ws_y; F.ws_stat = P.ws_stat; F.ws_w = P.ws_w; F.ws_p = P.ws_p;
   F.out_tokens = out_tokens; F.out_tau = out_tau; F.out_tv = P.out_tv; F.flags = P.flags;
-  F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.wv = P.wv; F.items = h->C * NWARP; F.vec16 = P.tma || P.vec16;
+  F.B = P.B; F.k = P.k; F.V = P.V; F.Vs = P.Vs; F.rbase = P.rbase; F.rextra = P.rextra; F.items = h->C * NWARP; F.vec16 = P.tma || P.vec16;
   F.tv_only = P.tv_only;
   F.lazy = lazy ? 1 : 0;
   h->finalize<<<(P.B + 7) / 8, 256, 0, s>>>(F);
@@ -1701,20 +1758,20 @@ int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) 
   }
   const long long Vs = ((long long)(vocab + C - 1) / C + epv - 1) / epv * epv;
   const long long nvec = Vs / epv;
-  const long long wv = (nvec + NWARP - 1) / NWARP;
-  const long long r_need = (wv + 31) / 32;
+  const long long nrounds = (nvec + 31) / 32;   // per CTA slice, split over the warps
+  const long long rbase = nrounds / NWARP, rextra = nrounds % NWARP;
+  const long long r_need = rbase + (rextra > 0 ? 1 : 0);
   int R = -1;
   for (int i = 0; i < N_R; ++i)
     if (R_CHOICES[i] >= r_need) { R = R_CHOICES[i]; break; }
   if (R < 0) return SV_ERR_SIZE;
   h.device = device; h.k = k; h.V = vocab; h.dtype = dtype;
-  h.C = C; h.Vs = (int)Vs; h.R = R; h.wv = (int)wv;
+  h.C = C; h.Vs = (int)Vs; h.R = R; h.rbase = (int)rbase; h.rextra = (int)rextra;
   h.tma_ok = ((size_t)vocab * es) % 16 == 0;
-  h.smem = SMALL_BYTES + (h.tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
+  h.smem = smem_bytes(R, h.tma_ok);
   if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
   else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
-  if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem) != cudaSuccess)
-    return SV_ERR_CUDA;
+  if (!set_smem_limit(h.kernel, R)) return SV_ERR_CUDA;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)C, 1, 1);
@@ -1780,8 +1837,9 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   }
   const long long Vs = ((long long)(vocab + C - 1) / C + epv - 1) / epv * epv;
   const long long nvec = Vs / epv;
-  const long long wv = (nvec + NWARP - 1) / NWARP;
-  const long long r_need = (wv + 31) / 32;
+  const long long nrounds = (nvec + 31) / 32;   // per CTA slice, split over the warps
+  const long long rbase = nrounds / NWARP, rextra = nrounds % NWARP;
+  const long long r_need = rbase + (rextra > 0 ? 1 : 0);
   int R = -1;
   for (int i = 0; i < N_R; ++i)
     if (R_CHOICES[i] >= r_need) { R = R_CHOICES[i]; break; }
@@ -1791,16 +1849,14 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   if (!h) return SV_ERR_ALLOC;
   if (cudaGetDevice(&h->device) != cudaSuccess) { free(h); return SV_ERR_CUDA; }
   h->max_batch = max_batch; h->k = k; h->V = vocab; h->dtype = logit_dtype; h->flags = flags;
-  h->C = C; h->Vs = (int)Vs; h->R = R; h->wv = (int)wv;
+  h->C = C; h->Vs = (int)Vs; h->R = R; h->rbase = (int)rbase; h->rextra = (int)rextra;
   h->tma_ok = ((size_t)vocab * es) % 16 == 0 && !(flags & SV_FLAG_NO_TMA);
-  h->smem = SMALL_BYTES + (h->tma_ok ? 2 * (size_t)NWARP * R * 32 * 16 : 0);
+  h->smem = smem_bytes(R, h->tma_ok);
   if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
   else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
   h->kernel_grad = logit_dtype == SV_FP32 ? pick_grad<float>(R) : pick_grad<__nv_bfloat16>(R);
-  if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
-      cudaFuncSetAttribute(h->kernel_ent, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
-      cudaFuncSetAttribute(h->kernel_grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess ||
-      cudaFuncSetAttribute(h->kernel_lazy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem) != cudaSuccess) {
+  if (!set_smem_limit(h->kernel, R) || !set_smem_limit(h->kernel_ent, R) || !set_smem_limit(h->kernel_grad, R) ||
+      !set_smem_limit(h->kernel_lazy, R)) {
     free_ctx(h);
     return SV_ERR_CUDA;
   }
@@ -1906,7 +1962,7 @@ static int verify_impl(spec_verify_t h, int batch, const void* target_logits, co
   P.out_ent_t = out_entropy_target; P.out_ent_d = out_entropy_draft;
   P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
   P.flags = h->d_flags;
-  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.rbase = h->rbase; P.rextra = h->rextra;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.vec16 = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.tma = bulk_ok && P.vec16;
@@ -1940,7 +1996,7 @@ int spec_verify_lazy(spec_verify_t h, int batch, const void* target_logits, cons
   P.uniforms = uniforms;
   P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
   P.flags = h->d_flags;
-  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.rbase = h->rbase; P.rextra = h->rextra;
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
@@ -1999,7 +2055,7 @@ int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype, const void
   P.ws_acc = (int32_t*)(scratch + L.acc); P.ws_y = (int32_t*)(scratch + L.y);
   P.ws_stat = (UnitStat*)(scratch + L.stat); P.ws_w = (float*)(scratch + L.w); P.ws_p = (float*)(scratch + L.p);
   P.flags = flags;
-  P.B = batch; P.k = k; P.V = vocab; P.Vs = h.Vs; P.wv = h.wv;
+  P.B = batch; P.k = k; P.V = vocab; P.Vs = h.Vs; P.rbase = h.rbase; P.rextra = h.rextra;
   P.units_per_chain = k + 1; P.tv_only = 0;
   P.tma = h.tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
@@ -2021,7 +2077,7 @@ int spec_verify_tv(spec_verify_t h, int batch, const void* target_logits, const 
   P.target = target_logits; P.draft = draft_logits; P.temperature = temperature; P.out_tv = out_tv;
   P.ws_acc = h->ws_acc; P.ws_y = h->ws_y; P.ws_stat = h->ws_stat; P.ws_w = h->ws_w; P.ws_p = h->ws_p;
   P.flags = h->d_flags;
-  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.rbase = h->rbase; P.rextra = h->rextra;
   P.units_per_chain = h->k; P.tv_only = 1;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
@@ -2046,7 +2102,7 @@ int spec_verify_loss_grad(spec_verify_t h, int batch, const void* target_logits,
   P.target = target_logits; P.draft = draft_logits; P.temperature = temperature;
   P.weights = weights; P.out_loss = out_loss; P.grad = grad_draft; P.loss_kind = loss_kind;
   P.flags = h->d_flags;
-  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.wv = h->wv;
+  P.B = batch; P.k = h->k; P.V = h->V; P.Vs = h->Vs; P.rbase = h->rbase; P.rextra = h->rextra;
   P.units_per_chain = h->k; P.tv_only = 1;
   P.tma = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
@@ -2134,7 +2190,9 @@ int spec_verify_selftest_wait(spec_verify_t h, int polls, long long* elapsed_cyc
     elapsed_cycles[0] = c[0];
     elapsed_cycles[1] = c[1];
   }
-  return spec_verify_get_error(h, nullptr);
+  int f[2] = {0, 0};   // read without clearing: the flag stays set until spec_verify_get_error
+  if (cudaMemcpy(f, h->d_flags, sizeof f, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
+  return f[1] ? SV_ERR_TIMEOUT : f[0] ? SV_ERR_DATA : SV_OK;
 }
 
 int spec_verify_info(spec_verify_t h, int* cluster_size, int* n_clusters, int* rounds, int* tma, int* launches_per_call) {

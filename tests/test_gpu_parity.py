@@ -237,3 +237,42 @@ def test_target_preservation_sampled_gpu(lib, oracle):
         exp = p[j] * sel.sum()
         keep = exp > 5
         assert scipy.stats.chisquare(counts[keep], exp[keep] * counts[keep].sum() / exp[keep].sum()).pvalue > 1e-4
+
+
+def _noalloc(lib, w, ins, out):
+    import ctypes
+    from speculative_decoding_verification_68_gb300 import _native
+    c = _native.load()
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    B = ins[0].shape[0]
+    dt = lib.SV_BF16 if w.dtype == si.BF16 else lib.SV_FP32
+    return c.spec_verify_noalloc(B, w.k, w.vocab, dt, *[p(t) for t in ins], p(out["tokens"]), p(out["tau"]),
+                                 p(out["p_draft"]), p(out["q_draft"]), p(out["tv"]),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def test_staged_and_plain_handles_coexist(lib):
+    """The kernels' shared-memory limit is shared by every handle of the same
+    shape: opening a handle with plain loads (SV_FLAG_NO_TMA) while a staging
+    handle is live must not lower it under the live handle, nor under the
+    allocation-free entry point's cached launch plan."""
+    w = si.C3_T06.scaled(batch=6)
+    b = si.generate(w)
+    ins = to_dev(b)
+    dt = torch.bfloat16
+    staged = lib.SpecVerifier(6, w.k, w.vocab, dt)
+    first = {k: t.cpu().numpy() for k, t in staged.verify(*ins, want_tv=True).items()}
+    na = staged.alloc_outputs(6, want_pq=True, want_tv=True)
+    assert _noalloc(lib, w, ins, na) == lib.SV_OK
+    plain = lib.SpecVerifier(6, w.k, w.vocab, dt, lib.SV_FLAG_NO_TMA)
+    again = staged.verify(*ins, want_tv=True)          # failed to launch when the limit was lowered
+    p_out = plain.verify(*ins, want_tv=True)
+    na2 = staged.alloc_outputs(6, want_pq=True, want_tv=True)
+    assert _noalloc(lib, w, ins, na2) == lib.SV_OK
+    torch.cuda.synchronize()
+    for res in (again, p_out, na, na2):
+        for key in first:
+            assert np.array_equal(first[key], res[key].cpu().numpy()), key
+    assert staged.get_error() == (lib.SV_OK, 0) and plain.get_error() == (lib.SV_OK, 0)
+    staged.close()
+    plain.close()
