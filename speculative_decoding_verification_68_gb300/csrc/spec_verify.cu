@@ -109,6 +109,8 @@ struct KParams {
   int grad_vec;              // gradient rows can take 16-byte stores
   // lazy verification
   int* ws_grab;              // chains handed out so far past the static ones (zeroed before the launch)
+  // verification kernel: tensor-memory columns each CTA allocates (a power of 2; CTAs per SM x this <= 512)
+  int tmem_cols;
 };
 
 struct alignas(16) X1 {       // one warp's part of the exchange (32 bytes)
@@ -139,6 +141,7 @@ struct Small {
   X1 x1[2][ITEMS_MAX];         // double-buffered exchange slots, written by peers
   int grab[2];                 // lazy verification: rank 0's counter value, per slot set
   Merged mg[2];                // merged row statistics (warp 0 to the other warps), per slot set
+  uint32_t tmem;               // the verification instance: this CTA's TMEM columns
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "bookkeeping area too small");
 
@@ -406,6 +409,73 @@ __device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr
   return l0 + h0;
 }
 
+// Tensor memory (TMEM, 256 KB per SM) holds each warp's target exponentials
+// from pass A until pass B: lanes 32 * (warp % 4) + [0, 32) (the quarter a
+// warp may address), EPV columns (32-bit) per register round, warps 4..7
+// after warps 0..3.  Stores and loads are asynchronous; the waits below order
+// them with the registers that feed or read them.
+template <int COLS_PER_WARP>
+__device__ __forceinline__ uint32_t tmem_warp_base(uint32_t base) {
+  const uint32_t warp = threadIdx.x >> 5;
+  return base + ((32u * (warp & 3u)) << 16) + (warp >> 2) * (uint32_t)COLS_PER_WARP;
+}
+__device__ __forceinline__ void tmem_st8(uint32_t ta, float e0, float e1, float e2, float e3, float e4, float e5,
+                                         float e6, float e7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(ta), "f"(e0), "f"(e1), "f"(e2), "f"(e3), "f"(e4), "f"(e5), "f"(e6), "f"(e7) : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t ta, float e0, float e1, float e2, float e3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+               ::"r"(ta), "f"(e0), "f"(e1), "f"(e2), "f"(e3) : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t ta, float (&e)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(e[0]), "=f"(e[1]), "=f"(e[2]), "=f"(e[3]), "=f"(e[4]), "=f"(e[5]), "=f"(e[6]), "=f"(e[7])
+               : "r"(ta) : "memory");
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t ta, float (&e)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(e[0]), "=f"(e[1]), "=f"(e[2]), "=f"(e[3]) : "r"(ta) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// rows_expsum, also storing every exponential in this warp's TMEM columns
+// (round j at column EPV * j), for pass B to read back instead of recomputing.
+template <typename Tl, int R>
+__device__ __forceinline__ float rows_expsum_store(const uint4 (&v)[R], u64 cc, u64 nr, bool last, uint32_t tm) {
+  u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (j == R - 1 && !last) break;
+    float x0, x1, x2, x3;
+    if constexpr (sizeof(Tl) == 4) {
+      upk(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr), x0, x1);
+      upk(fma2(pk(__uint_as_float(v[j].z), __uint_as_float(v[j].w)), cc, nr), x2, x3);
+      const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+      tmem_st4(tm + 4u * j, e0, e1, e2, e3);
+      if (j & 1) { a2 = add2(a2, pk(e0, e1)); a3 = add2(a3, pk(e2, e3)); }
+      else { a0 = add2(a0, pk(e0, e1)); a1 = add2(a1, pk(e2, e3)); }
+    } else {
+      float x4, x5, x6, x7;
+      upk(fma2(pk(bf_lo(v[j].x), bf_hi(v[j].x)), cc, nr), x0, x1);
+      upk(fma2(pk(bf_lo(v[j].y), bf_hi(v[j].y)), cc, nr), x2, x3);
+      upk(fma2(pk(bf_lo(v[j].z), bf_hi(v[j].z)), cc, nr), x4, x5);
+      upk(fma2(pk(bf_lo(v[j].w), bf_hi(v[j].w)), cc, nr), x6, x7);
+      const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
+      const float e4 = ex2(x4), e5 = ex2(x5), e6 = ex2(x6), e7 = ex2(x7);
+      tmem_st8(tm + 8u * j, e0, e1, e2, e3, e4, e5, e6, e7);
+      a0 = add2(a0, pk(e0, e1));
+      a1 = add2(a1, pk(e2, e3));
+      a2 = add2(a2, pk(e4, e5));
+      a3 = add2(a3, pk(e6, e7));
+    }
+  }
+  float l0, h0;
+  upk(add2(add2(a0, a1), add2(a2, a3)), l0, h0);
+  return l0 + h0;
+}
+
 // As rows_expsum, and also sum e*a over the same elements, e = 2^a with
 // a = z*c + nref (the log2-domain logit relative to the reference): the
 // second moment the row entropy needs, H = ln S - ln2 * (sum e*a) / S.
@@ -416,8 +486,11 @@ __device__ __forceinline__ u64 clamp_m127(u64 x) {
   upk(x, lo, hi);
   return pk(fmaxf(lo, -127.0f), fmaxf(hi, -127.0f));
 }
-template <typename Tl, int R>
-__device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, bool last, float& ea) {
+// (With STORE, every exponential also goes to this warp's TMEM columns, as in
+// rows_expsum_store.)
+template <typename Tl, int R, bool STORE = false>
+__device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, bool last, float& ea,
+                                                 uint32_t tm = 0) {
   u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
   u64 m0 = 0ull, m1 = 0ull, m2 = 0ull, m3 = 0ull;
 #pragma unroll
@@ -431,6 +504,12 @@ __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u6
       upk(x0, p0, p1);
       upk(x1, p2, p3);
       const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3));
+      if constexpr (STORE) {
+        float f0, f1, f2, f3;
+        upk(e0, f0, f1);
+        upk(e1, f2, f3);
+        tmem_st4(tm + 4u * j, f0, f1, f2, f3);
+      }
       if (j & 1) { a2 = add2(a2, e0); a3 = add2(a3, e1); m2 = fma2(e0, x0, m2); m3 = fma2(e1, x1, m3); }
       else { a0 = add2(a0, e0); a1 = add2(a1, e1); m0 = fma2(e0, x0, m0); m1 = fma2(e1, x1, m1); }
     } else {
@@ -444,6 +523,14 @@ __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u6
       upk(x2, p4, p5);
       upk(x3, p6, p7);
       const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3)), e2 = pk(ex2(p4), ex2(p5)), e3 = pk(ex2(p6), ex2(p7));
+      if constexpr (STORE) {
+        float f0, f1, f2, f3, f4, f5, f6, f7;
+        upk(e0, f0, f1);
+        upk(e1, f2, f3);
+        upk(e2, f4, f5);
+        upk(e3, f6, f7);
+        tmem_st8(tm + 8u * j, f0, f1, f2, f3, f4, f5, f6, f7);
+      }
       a0 = add2(a0, e0); a1 = add2(a1, e1); a2 = add2(a2, e2); a3 = add2(a3, e3);
       m0 = fma2(e0, x0, m0); m1 = fma2(e1, x1, m1); m2 = fma2(e2, x2, m2); m3 = fma2(e3, x3, m3);
     }
@@ -552,7 +639,8 @@ template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
 __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
-                                             const float T, const int x, const bool carry = false) {
+                                             const float T, const int x, const bool carry = false,
+                                             const uint32_t tm = 0) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -665,7 +753,8 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     if constexpr (ENT) {   // the index fields carry sum e*a for sampling units
       float ea_t = 0.0f, ea_d = 0.0f;
-      mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), last, ea_t);
+      if (PAIR) mine.s_t = rows_expsum_ent<Tl, R, true>(rt, cc, pk(-rwt, -rwt), last, ea_t, tm);
+      else mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), last, ea_t);
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
@@ -682,7 +771,9 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       mine.s_t = v0; mine.s_d = v1;
       mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
     } else {
-      mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
+      // keep the target exponentials of a row pair in TMEM for pass B
+      mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R>(rt, cc, pk(-rwt, -rwt), last, tm)
+                                   : rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
@@ -833,16 +924,52 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
 
   // ---------------- pass B: residual mass of this warp's range
   const u64 cc = pk(c, c);
-  const u64 nrt = pk(-M.R_t, -M.R_t), nrd = pk(-M.R_d, -M.R_d);
-  const float nr = -M.r;
-  float w0 = 0.0f, w1 = 0.0f;
+  float wwarp;
+  {
+    // The target exponentials e_t = 2^(z_t c - ref_t) come back from TMEM
+    // (pass A stored them, relative to this warp's reference ref_t); the draft
+    // ones are recomputed relative to this warp's draft reference ref_d, as in
+    // pass A.  With s_t = 2^(ref_t - R_t) and s_d = 2^(ref_d - R_d) (exact
+    // powers of 2), the weight on the row references is
+    //   max(0, s_t e_t - r s_d e_d) = s_t * sat(e_t - r (s_d / s_t) e_d),
+    // the clamp being exact because e_t <= 1; identical rows give exactly 0.
+    float wacc = 0.0f;
+    if (mine.ref_t != NO_REF) {   // else the warp's target range is all masked: no residual
+      constexpr int EPV = Lay<Tl>::EPV;
+      const int e_sc = mine.ref_d == NO_REF ? 0 : (mine.ref_d - (int)M.R_d) - (mine.ref_t - M.IR_t);
+      const float sc = e_sc < -126 ? 0.0f : e_sc > 127 ? INFINITY : __int_as_float((e_sc + 127) << 23);
+      const float nrs = mine.ref_d == NO_REF ? 0.0f : -M.r * sc;
+      const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
+      const u64 nrdw = pk(-rwd, -rwd);
+      tmem_wait_st();   // pass A's stores are complete
+      u64 a0 = 0ull, a1 = 0ull;
 #pragma unroll
-  for (int j = 0; j < R; ++j) {
-    if (j == R - 1 && !last) break;
-    const float wj = vec_weight_sum<Tl, true>(rt[j], rd[j], cc, nrt, nrd, nr);
-    if (j & 1) w1 += wj; else w0 += wj;
+      for (int j = 0; j < R; ++j) {
+        if (j == R - 1 && !last) break;
+        float et[EPV];
+        if constexpr (EPV == 8) tmem_ld8(tm + 8u * j, et);
+        else tmem_ld4(tm + 4u * j, et);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < EPV / 2; ++q) {
+          const uint32_t wd = q == 0 ? rd[j].x : q == 1 ? rd[j].y : q == 2 ? rd[j].z : rd[j].w;
+          float ad0, ad1;
+          if constexpr (EPV == 8) upk(fma2(pk(bf_lo(wd), bf_hi(wd)), cc, nrdw), ad0, ad1);
+          else {
+            const uint32_t wd1 = q == 0 ? rd[j].y : rd[j].w;
+            const uint32_t wd0 = q == 0 ? rd[j].x : rd[j].z;
+            upk(fma2(pk(__uint_as_float(wd0), __uint_as_float(wd1)), cc, nrdw), ad0, ad1);
+          }
+          const u64 w = pk(fma_sat(ex2(ad0), nrs, et[2 * q]), fma_sat(ex2(ad1), nrs, et[2 * q + 1]));
+          if (q & 1) a1 = add2(a1, w); else a0 = add2(a0, w);
+        }
+      }
+      float l, h;
+      upk(add2(a0, a1), l, h);
+      wacc = (l + h) * pow2_diff(mine.ref_t, M.IR_t);
+    }
+    wwarp = warp_sum_f32(wacc);
   }
-  const float wwarp = warp_sum_f32(w0 + w1);
   if (lane == 0) P.ws_w[item] = wwarp;
   if (!LAZY && own_x && tid == 0) {   // accept test at the drafted token
     const float lpx = fmaf(S.gz_t, c, -M.R_t), lqx = fmaf(S.gz_d, c, -M.R_d);
@@ -883,9 +1010,18 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
     S.cnt = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  constexpr bool USE_TMEM = true;   // target exponentials wait in TMEM from pass A to pass B
+  if (USE_TMEM && warp == 0) {   // the host keeps CTAs per SM x tmem_cols within the SM's 512 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem)),
+                 "r"(P.tmem_cols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (USE_TMEM) asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (USE_TMEM) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   cluster_sync_all();   // every peer's shared memory is live before the first remote store
+  const uint32_t tm = USE_TMEM ? tmem_warp_base<Lay<Tl>::EPV * R>(S.tmem) : 0u;
 
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
@@ -923,10 +1059,10 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
       int cont;
       if (cur.ipos < k)
         cont = process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
-                                                     P.tma && has_next, T, x, carry);
+                                                     P.tma && has_next, T, x, carry, tm);
       else
         cont = process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
-                                                      P.tma && has_next, T, x, carry);
+                                                      P.tma && has_next, T, x, carry, tm);
       phase ^= 1u;
       if (carry) {   // this unit's exchange brought the new reserve
         reserve = chain_or_none(first + (unsigned long long)(unsigned)S.mg[(n1 - 1) & 1].grab);
@@ -954,10 +1090,21 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
       const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
       const bool tma_next = P.tma && has_next;
       if (cur.ipos < k)
-        process_unit<Tl, R, true, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+        process_unit<Tl, R, true, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
+                                              false, tm);
       else
-        process_unit<Tl, R, false, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x);
+        process_unit<Tl, R, false, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
+                                               false, tm);
       cur = next;
+    }
+  }
+  if (USE_TMEM) {   // every TMEM access of the CTA is complete before its columns are freed
+    tmem_wait_st();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem), "r"(P.tmem_cols) : "memory");
     }
   }
   cluster_sync_all();   // no CTA leaves while a peer could still address its shared memory
@@ -1587,7 +1734,11 @@ struct spec_verify_ctx {
   int max_batch, k, V, dtype;
   unsigned flags;
   int C, Vs, R, rbase, rextra, n_clusters, tma_ok;
-  size_t smem;
+  size_t smem;               // dynamic shared memory of the fused kernels
+  size_t smem_verify;        // that of the verification, entropy and lazy instances (padded if their
+  size_t smem_ent;           // TMEM columns need it)
+  size_t smem_lazy;
+  int tmem_cols;             // TMEM columns per CTA of those instances
   FusedFn kernel;
   FusedFn kernel_ent;        // the same kernel that also writes row entropies
   int n_clusters_ent;
@@ -1634,6 +1785,89 @@ static bool set_smem_limit(FusedFn f, int R) {
   return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(R, true)) == cudaSuccess;
 }
 
+// Never launched: the occupancy calculation reports the number of clusters of
+// C CTAs that fit when each SM holds a given number of CTAs, set through this
+// kernel's dynamic shared memory.
+__global__ void sv_cluster_fit_kernel(int*) {}
+
+// Launch plan of the verification instance (the kernel that keeps target
+// exponentials in TMEM): dynamic shared memory, TMEM columns per CTA, and the
+// number of co-resident clusters.
+//  - Each CTA allocates the power of 2 at or above the 2 EPV R columns its
+//    warps use (two warps per lane quarter) and holds them for the whole
+//    kernel.  The CTAs an SM holds at once must fit in its 512 columns, or one
+//    could wait for columns that its own cluster's progress is needed to free;
+//    the shared-memory request is padded until the SM's other limits allow no
+//    more CTAs than that.
+//  - The occupancy calculation assumes that a kernel using TMEM owns the SM
+//    (it reports one CTA per SM), while the hardware schedules such CTAs by
+//    registers, shared memory and threads like any other (measured: two CTAs
+//    of 256 columns on every SM).  So CTAs per SM are counted here from those
+//    limits, and the number of clusters that fit with that many CTAs per SM is
+//    taken from a stand-in kernel without TMEM.
+static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t smem_staged, size_t* smem,
+                       int* tmem_cols, int* n_clusters) {
+  int dev = 0, optin = 0, sm_smem = 0, sm_regs = 0, sm_thr = 0, sm_blocks = 0, reserved = 0;
+  cudaFuncAttributes fa;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_thr, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, f) != cudaSuccess)
+    return SV_ERR_CUDA;
+  optin -= (int)fa.sharedSizeBytes;   // the limit covers dynamic shared memory only
+  int need = 32;
+  while (need < 2 * epv * R) need <<= 1;
+  const int tmem_ctas = 512 / need;
+  // registers are allocated per warp in multiples of 256
+  const long long regs_cta = (long long)((fa.numRegs * 32 + 255) / 256 * 256) * (NT / 32);
+  size_t sm = smem0;
+  int ctas = 0;
+  for (;;) {
+    const long long by_smem = (long long)sm_smem / ((long long)sm + fa.sharedSizeBytes + reserved);
+    long long c = sm_regs / regs_cta;
+    c = c < by_smem ? c : by_smem;
+    c = c < sm_thr / NT ? c : sm_thr / NT;
+    c = c < sm_blocks ? c : sm_blocks;
+    if (c <= 0) return SV_ERR_SIZE;
+    if (c <= tmem_ctas) { ctas = (int)c; break; }
+    sm += 4096;   // fewer CTAs per SM
+    if (sm > (size_t)optin) return SV_ERR_SIZE;
+  }
+  // the opt-in limit is shared by every handle of this kernel: raised to the
+  // largest request any plan makes (the staged one, or a padded one), never lowered
+  const size_t lim = sm > smem_staged ? sm : smem_staged;
+  if ((int)lim > fa.maxDynamicSharedSizeBytes &&
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lim) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const int fit_smem = sm_smem / ctas - reserved;   // the stand-in then holds `ctas` CTAs per SM
+  if (cudaFuncSetAttribute(sv_cluster_fit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fit_smem) != cudaSuccess)
+    return SV_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)C, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)fit_smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)C;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int per_sm = 0, n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv_cluster_fit_kernel, NT, (size_t)fit_smem) != cudaSuccess ||
+      per_sm != ctas || cudaOccupancyMaxActiveClusters(&n, sv_cluster_fit_kernel, &cfg) != cudaSuccess || n <= 0)
+    return SV_ERR_CUDA;
+  *smem = sm;
+  *tmem_cols = need;
+  *n_clusters = n;
+  return SV_OK;
+}
+
 static void free_ctx(spec_verify_ctx* h) {
   if (!h) return;
   void* ptrs[] = {h->ws_acc, h->ws_y, h->ws_stat, h->ws_w, h->ws_p, h->d_flags, h->ws_grab, h->st_target, h->st_draft, h->st_tokens, h->st_temp,
@@ -1660,7 +1894,7 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)(grid_clusters * h->C), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = h->smem;
+  cfg.dynamicSmemBytes = grad ? h->smem : lazy ? h->smem_lazy : ent ? h->smem_ent : h->smem_verify;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1669,7 +1903,9 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : lazy ? h->kernel_lazy : ent ? h->kernel_ent : h->kernel, P) !=
+  KParams Q = P;
+  Q.tmem_cols = h->tmem_cols;
+  if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : lazy ? h->kernel_lazy : ent ? h->kernel_ent : h->kernel, Q) !=
       cudaSuccess)
     return SV_ERR_CUDA;
   if (timed) {
@@ -1771,25 +2007,12 @@ int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) 
   h.smem = smem_bytes(R, h.tma_ok);
   if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
   else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
-  if (!set_smem_limit(h.kernel, R)) return SV_ERR_CUDA;
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)C, 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = h.smem;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = (unsigned)C;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, h.kernel, &cfg) != cudaSuccess || n <= 0) {
+  const int rc = plan_verify(h.kernel, R, epv, C, h.smem, smem_bytes(R, true), &h.smem_verify, &h.tmem_cols,
+                             &h.n_clusters);
+  if (rc != SV_OK) {
     cudaGetLastError();
-    return SV_ERR_CUDA;
+    return rc;
   }
-  h.n_clusters = n;
   for (int i = 0; i < NOALLOC_PLANS; ++i) {
     if (!g_noalloc_plans[i].used) {
       g_noalloc_plans[i].used = true;
@@ -1855,8 +2078,7 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
   if (logit_dtype == SV_FP32) pick_kernels<float>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
   else pick_kernels<__nv_bfloat16>(R, h->kernel, h->kernel_ent, h->kernel_lazy, h->finalize);
   h->kernel_grad = logit_dtype == SV_FP32 ? pick_grad<float>(R) : pick_grad<__nv_bfloat16>(R);
-  if (!set_smem_limit(h->kernel, R) || !set_smem_limit(h->kernel_ent, R) || !set_smem_limit(h->kernel_grad, R) ||
-      !set_smem_limit(h->kernel_lazy, R)) {
+  if (!set_smem_limit(h->kernel_grad, R)) {
     free_ctx(h);
     return SV_ERR_CUDA;
   }
@@ -1873,19 +2095,24 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0, ne = 0, ng = 0, nl = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, h->kernel, &cfg) != cudaSuccess || n <= 0 ||
-        cudaOccupancyMaxActiveClusters(&ne, h->kernel_ent, &cfg) != cudaSuccess || ne <= 0 ||
-        cudaOccupancyMaxActiveClusters(&ng, h->kernel_grad, &cfg) != cudaSuccess || ng <= 0 ||
-        cudaOccupancyMaxActiveClusters(&nl, h->kernel_lazy, &cfg) != cudaSuccess || nl <= 0) {
+    int ng = 0, te = 0, tl = 0;
+    int rc = plan_verify(h->kernel, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_verify, &h->tmem_cols,
+                         &h->n_clusters);
+    if (rc == SV_OK)
+      rc = plan_verify(h->kernel_ent, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_ent, &te, &h->n_clusters_ent);
+    if (rc == SV_OK)
+      rc = plan_verify(h->kernel_lazy, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_lazy, &tl, &h->n_clusters_lazy);
+    if (rc != SV_OK) {
+      cudaGetLastError();
+      free_ctx(h);
+      return rc;
+    }
+    if (cudaOccupancyMaxActiveClusters(&ng, h->kernel_grad, &cfg) != cudaSuccess || ng <= 0) {
       cudaGetLastError();
       free_ctx(h);
       return SV_ERR_CUDA;
     }
-    h->n_clusters = n;
-    h->n_clusters_ent = ne;
     h->n_clusters_grad = ng;
-    h->n_clusters_lazy = nl;
   }
   const size_t mb = (size_t)(max_batch > 0 ? max_batch : 1);
   bool ok = cudaMalloc(&h->ws_acc, mb * k * sizeof(int32_t)) == cudaSuccess &&
