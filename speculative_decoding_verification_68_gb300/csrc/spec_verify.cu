@@ -409,15 +409,24 @@ __device__ __forceinline__ float rows_expsum(const uint4 (&v)[R], u64 cc, u64 nr
   return l0 + h0;
 }
 
-// Tensor memory (TMEM, 256 KB per SM) holds each warp's target exponentials
-// from pass A until pass B: lanes 32 * (warp % 4) + [0, 32) (the quarter a
-// warp may address), EPV columns (32-bit) per register round, warps 4..7
-// after warps 0..3.  Stores and loads are asynchronous; the waits below order
-// them with the registers that feed or read them.
-template <int COLS_PER_WARP>
+// Tensor memory (TMEM, 256 KB per SM: 128 lanes x 512 32-bit columns) holds
+// each warp's exponentials from pass A until pass B: lanes 32 * (warp % 4) +
+// [0, 32) (the quarter a warp may address), EPV columns per register round,
+// warps 4..7 after warps 0..3.  A warp keeps its R target rounds and then the
+// draft exponentials of its first DR rounds, DR as many as fit in the CTA's
+// share of the columns at the CTAs per SM the kernel is compiled for (two up
+// to R = 10, else one).  Stores and loads are asynchronous; the waits below
+// order them with the registers that feed or read them.
+__host__ __device__ constexpr int tmem_draft_rounds(int epv, int R) {
+  return (256 / (R <= 10 ? 2 : 1) - epv * R) / epv < 0 ? 0
+       : (256 / (R <= 10 ? 2 : 1) - epv * R) / epv > R ? R
+       : (256 / (R <= 10 ? 2 : 1) - epv * R) / epv;   // 256 / CTAs per SM = columns of warps 0..3
+}
+__host__ __device__ constexpr int tmem_cols_per_warp(int epv, int R) { return epv * (R + tmem_draft_rounds(epv, R)); }
+template <int EPV, int R>
 __device__ __forceinline__ uint32_t tmem_warp_base(uint32_t base) {
   const uint32_t warp = threadIdx.x >> 5;
-  return base + ((32u * (warp & 3u)) << 16) + (warp >> 2) * (uint32_t)COLS_PER_WARP;
+  return base + ((32u * (warp & 3u)) << 16) + (warp >> 2) * (uint32_t)tmem_cols_per_warp(EPV, R);
 }
 __device__ __forceinline__ void tmem_st8(uint32_t ta, float e0, float e1, float e2, float e3, float e4, float e5,
                                          float e6, float e7) {
@@ -440,9 +449,10 @@ __device__ __forceinline__ void tmem_ld4(uint32_t ta, float (&e)[4]) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// rows_expsum, also storing every exponential in this warp's TMEM columns
-// (round j at column EPV * j), for pass B to read back instead of recomputing.
-template <typename Tl, int R>
+// rows_expsum, also storing the exponentials of rounds j < NSTORE in this
+// warp's TMEM columns (round j at column EPV * j from tm), for pass B to read
+// back instead of recomputing.
+template <typename Tl, int R, int NSTORE>
 __device__ __forceinline__ float rows_expsum_store(const uint4 (&v)[R], u64 cc, u64 nr, bool last, uint32_t tm) {
   u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
 #pragma unroll
@@ -453,7 +463,7 @@ __device__ __forceinline__ float rows_expsum_store(const uint4 (&v)[R], u64 cc, 
       upk(fma2(pk(__uint_as_float(v[j].x), __uint_as_float(v[j].y)), cc, nr), x0, x1);
       upk(fma2(pk(__uint_as_float(v[j].z), __uint_as_float(v[j].w)), cc, nr), x2, x3);
       const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
-      tmem_st4(tm + 4u * j, e0, e1, e2, e3);
+      if (j < NSTORE) tmem_st4(tm + 4u * j, e0, e1, e2, e3);
       if (j & 1) { a2 = add2(a2, pk(e0, e1)); a3 = add2(a3, pk(e2, e3)); }
       else { a0 = add2(a0, pk(e0, e1)); a1 = add2(a1, pk(e2, e3)); }
     } else {
@@ -464,7 +474,7 @@ __device__ __forceinline__ float rows_expsum_store(const uint4 (&v)[R], u64 cc, 
       upk(fma2(pk(bf_lo(v[j].w), bf_hi(v[j].w)), cc, nr), x6, x7);
       const float e0 = ex2(x0), e1 = ex2(x1), e2 = ex2(x2), e3 = ex2(x3);
       const float e4 = ex2(x4), e5 = ex2(x5), e6 = ex2(x6), e7 = ex2(x7);
-      tmem_st8(tm + 8u * j, e0, e1, e2, e3, e4, e5, e6, e7);
+      if (j < NSTORE) tmem_st8(tm + 8u * j, e0, e1, e2, e3, e4, e5, e6, e7);
       a0 = add2(a0, pk(e0, e1));
       a1 = add2(a1, pk(e2, e3));
       a2 = add2(a2, pk(e4, e5));
@@ -488,7 +498,7 @@ __device__ __forceinline__ u64 clamp_m127(u64 x) {
 }
 // (With STORE, every exponential also goes to this warp's TMEM columns, as in
 // rows_expsum_store.)
-template <typename Tl, int R, bool STORE = false>
+template <typename Tl, int R, int NSTORE = 0>
 __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, bool last, float& ea,
                                                  uint32_t tm = 0) {
   u64 a0 = 0ull, a1 = 0ull, a2 = 0ull, a3 = 0ull;
@@ -504,7 +514,7 @@ __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u6
       upk(x0, p0, p1);
       upk(x1, p2, p3);
       const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3));
-      if constexpr (STORE) {
+      if (j < NSTORE) {
         float f0, f1, f2, f3;
         upk(e0, f0, f1);
         upk(e1, f2, f3);
@@ -523,7 +533,7 @@ __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u6
       upk(x2, p4, p5);
       upk(x3, p6, p7);
       const u64 e0 = pk(ex2(p0), ex2(p1)), e1 = pk(ex2(p2), ex2(p3)), e2 = pk(ex2(p4), ex2(p5)), e3 = pk(ex2(p6), ex2(p7));
-      if constexpr (STORE) {
+      if (j < NSTORE) {
         float f0, f1, f2, f3, f4, f5, f6, f7;
         upk(e0, f0, f1);
         upk(e1, f2, f3);
@@ -753,12 +763,13 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     if constexpr (ENT) {   // the index fields carry sum e*a for sampling units
       float ea_t = 0.0f, ea_d = 0.0f;
-      if (PAIR) mine.s_t = rows_expsum_ent<Tl, R, true>(rt, cc, pk(-rwt, -rwt), last, ea_t, tm);
+      if (PAIR) mine.s_t = rows_expsum_ent<Tl, R, R>(rt, cc, pk(-rwt, -rwt), last, ea_t, tm);
       else mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), last, ea_t);
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = rows_expsum_ent<Tl, R>(rd, cc, pk(-rwd, -rwd), last, ea_d);
+        mine.s_d = rows_expsum_ent<Tl, R, tmem_draft_rounds(Lay<Tl>::EPV, R)>(rd, cc, pk(-rwd, -rwd), last, ea_d,
+                                                                              tm + Lay<Tl>::EPV * R);
       }
       float v0 = mine.s_t, v1 = mine.s_d, v2 = ea_t, v3 = ea_d;
 #pragma unroll
@@ -772,12 +783,13 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
     } else {
       // keep the target exponentials of a row pair in TMEM for pass B
-      mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R>(rt, cc, pk(-rwt, -rwt), last, tm)
+      mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R, R>(rt, cc, pk(-rwt, -rwt), last, tm)
                                    : rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, cc, pk(-rwd, -rwd), last));
+        mine.s_d = warp_sum_f32(rows_expsum_store<Tl, R, tmem_draft_rounds(Lay<Tl>::EPV, R)>(
+            rd, cc, pk(-rwd, -rwd), last, tm + Lay<Tl>::EPV * R));
       }
     }
   }
@@ -942,27 +954,47 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
       const u64 nrdw = pk(-rwd, -rwd);
       tmem_wait_st();   // pass A's stores are complete
+      constexpr int ndr = tmem_draft_rounds(EPV, R);   // rounds whose draft exponentials were kept too
+      const uint32_t tmd = tm + EPV * R;
       u64 a0 = 0ull, a1 = 0ull;
+      // one round: the weights of its EPV positions, from e_t and e_d (kept, or recomputed as in pass A)
+      auto round_w = [&](int j, const float (&et)[EPV], const float (&ed)[EPV], bool kept) {
+#pragma unroll
+        for (int q = 0; q < EPV / 2; ++q) {
+          float e0, e1;
+          if (kept) {
+            e0 = ed[2 * q];
+            e1 = ed[2 * q + 1];
+          } else {
+            float ad0, ad1;
+            if constexpr (EPV == 8) {
+              const uint32_t wd = q == 0 ? rd[j].x : q == 1 ? rd[j].y : q == 2 ? rd[j].z : rd[j].w;
+              upk(fma2(pk(bf_lo(wd), bf_hi(wd)), cc, nrdw), ad0, ad1);
+            } else {
+              const uint32_t wd0 = q == 0 ? rd[j].x : rd[j].z, wd1 = q == 0 ? rd[j].y : rd[j].w;
+              upk(fma2(pk(__uint_as_float(wd0), __uint_as_float(wd1)), cc, nrdw), ad0, ad1);
+            }
+            e0 = ex2(ad0);
+            e1 = ex2(ad1);
+          }
+          const u64 w = pk(fma_sat(e0, nrs, et[2 * q]), fma_sat(e1, nrs, et[2 * q + 1]));
+          if (q & 1) a1 = add2(a1, w); else a0 = add2(a0, w);
+        }
+      };
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         if (j == R - 1 && !last) break;
-        float et[EPV];
-        if constexpr (EPV == 8) tmem_ld8(tm + 8u * j, et);
-        else tmem_ld4(tm + 4u * j, et);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < EPV / 2; ++q) {
-          const uint32_t wd = q == 0 ? rd[j].x : q == 1 ? rd[j].y : q == 2 ? rd[j].z : rd[j].w;
-          float ad0, ad1;
-          if constexpr (EPV == 8) upk(fma2(pk(bf_lo(wd), bf_hi(wd)), cc, nrdw), ad0, ad1);
-          else {
-            const uint32_t wd1 = q == 0 ? rd[j].y : rd[j].w;
-            const uint32_t wd0 = q == 0 ? rd[j].x : rd[j].z;
-            upk(fma2(pk(__uint_as_float(wd0), __uint_as_float(wd1)), cc, nrdw), ad0, ad1);
-          }
-          const u64 w = pk(fma_sat(ex2(ad0), nrs, et[2 * q]), fma_sat(ex2(ad1), nrs, et[2 * q + 1]));
-          if (q & 1) a1 = add2(a1, w); else a0 = add2(a0, w);
+        const bool kept = j < ndr;
+        float et[EPV], ed[EPV];
+        if constexpr (EPV == 8) {
+          tmem_ld8(tm + 8u * j, et);
+          if (kept) tmem_ld8(tmd + 8u * j, ed);
+        } else {
+          tmem_ld4(tm + 4u * j, et);
+          if (kept) tmem_ld4(tmd + 4u * j, ed);
         }
+        tmem_wait_ld();
+        round_w(j, et, ed, kept);
       }
       float l, h;
       upk(add2(a0, a1), l, h);
@@ -1021,7 +1053,7 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
   __syncthreads();
   if (USE_TMEM) asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   cluster_sync_all();   // every peer's shared memory is live before the first remote store
-  const uint32_t tm = USE_TMEM ? tmem_warp_base<Lay<Tl>::EPV * R>(S.tmem) : 0u;
+  const uint32_t tm = USE_TMEM ? tmem_warp_base<Lay<Tl>::EPV, R>(S.tmem) : 0u;
 
   unsigned phase = 0;
   int n1 = 0;   // exchanges performed (selects the slot set)
@@ -1729,16 +1761,19 @@ void pick_kernels(int r, FusedFn& f, FusedFn& fe, FusedFn& fl, FinalFn& g) {
 }  // namespace
 
 // ------------------------------------------------------------------ host side
+// launch plan of one TMEM-using verification instance
+struct VerifyPlan {
+  size_t smem;        // dynamic shared memory (padded above the staged size when TMEM columns need it)
+  int tmem_cols;      // TMEM columns per CTA
+};
+
 struct spec_verify_ctx {
   int device;
   int max_batch, k, V, dtype;
   unsigned flags;
   int C, Vs, R, rbase, rextra, n_clusters, tma_ok;
   size_t smem;               // dynamic shared memory of the fused kernels
-  size_t smem_verify;        // that of the verification, entropy and lazy instances (padded if their
-  size_t smem_ent;           // TMEM columns need it)
-  size_t smem_lazy;
-  int tmem_cols;             // TMEM columns per CTA of those instances
+  VerifyPlan plan_v, plan_ent, plan_lazy;   // the verification, entropy and lazy instances
   FusedFn kernel;
   FusedFn kernel_ent;        // the same kernel that also writes row entropies
   int n_clusters_ent;
@@ -1805,8 +1840,8 @@ __global__ void sv_cluster_fit_kernel(int*) {}
 //    of 256 columns on every SM).  So CTAs per SM are counted here from those
 //    limits, and the number of clusters that fit with that many CTAs per SM is
 //    taken from a stand-in kernel without TMEM.
-static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t smem_staged, size_t* smem,
-                       int* tmem_cols, int* n_clusters) {
+static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t smem_staged, VerifyPlan* plan,
+                       int* n_clusters) {
   int dev = 0, optin = 0, sm_smem = 0, sm_regs = 0, sm_thr = 0, sm_blocks = 0, reserved = 0;
   cudaFuncAttributes fa;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1819,8 +1854,8 @@ static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t sm
       cudaFuncGetAttributes(&fa, f) != cudaSuccess)
     return SV_ERR_CUDA;
   optin -= (int)fa.sharedSizeBytes;   // the limit covers dynamic shared memory only
-  int need = 32;
-  while (need < 2 * epv * R) need <<= 1;
+  int need = 32;   // warps 0..3 and 4..7 each take tmem_cols_per_warp columns
+  while (need < 2 * tmem_cols_per_warp(epv, R)) need <<= 1;
   const int tmem_ctas = 512 / need;
   // registers are allocated per warp in multiples of 256
   const long long regs_cta = (long long)((fa.numRegs * 32 + 255) / 256 * 256) * (NT / 32);
@@ -1862,8 +1897,8 @@ static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t sm
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv_cluster_fit_kernel, NT, (size_t)fit_smem) != cudaSuccess ||
       per_sm != ctas || cudaOccupancyMaxActiveClusters(&n, sv_cluster_fit_kernel, &cfg) != cudaSuccess || n <= 0)
     return SV_ERR_CUDA;
-  *smem = sm;
-  *tmem_cols = need;
+  plan->smem = sm;
+  plan->tmem_cols = need;
   *n_clusters = n;
   return SV_OK;
 }
@@ -1894,7 +1929,8 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)(grid_clusters * h->C), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = grad ? h->smem : lazy ? h->smem_lazy : ent ? h->smem_ent : h->smem_verify;
+  const VerifyPlan& vp = lazy ? h->plan_lazy : ent ? h->plan_ent : h->plan_v;
+  cfg.dynamicSmemBytes = grad ? h->smem : vp.smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1904,7 +1940,7 @@ static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, c
   cfg.attrs = at;
   cfg.numAttrs = 1;
   KParams Q = P;
-  Q.tmem_cols = h->tmem_cols;
+  Q.tmem_cols = grad ? 0 : vp.tmem_cols;
   if (cudaLaunchKernelEx(&cfg, grad ? h->kernel_grad : lazy ? h->kernel_lazy : ent ? h->kernel_ent : h->kernel, Q) !=
       cudaSuccess)
     return SV_ERR_CUDA;
@@ -2007,8 +2043,7 @@ int noalloc_plan(int device, int k, int vocab, int dtype, spec_verify_ctx& out) 
   h.smem = smem_bytes(R, h.tma_ok);
   if (dtype == SV_FP32) pick_kernels<float>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
   else pick_kernels<__nv_bfloat16>(R, h.kernel, h.kernel_ent, h.kernel_lazy, h.finalize);
-  const int rc = plan_verify(h.kernel, R, epv, C, h.smem, smem_bytes(R, true), &h.smem_verify, &h.tmem_cols,
-                             &h.n_clusters);
+  const int rc = plan_verify(h.kernel, R, epv, C, h.smem, smem_bytes(R, true), &h.plan_v, &h.n_clusters);
   if (rc != SV_OK) {
     cudaGetLastError();
     return rc;
@@ -2095,13 +2130,12 @@ int spec_verify_init(spec_verify_t* out, int max_batch, int k, int vocab, int lo
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int ng = 0, te = 0, tl = 0;
-    int rc = plan_verify(h->kernel, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_verify, &h->tmem_cols,
-                         &h->n_clusters);
+    int ng = 0;
+    int rc = plan_verify(h->kernel, R, epv, C, h->smem, smem_bytes(R, true), &h->plan_v, &h->n_clusters);
     if (rc == SV_OK)
-      rc = plan_verify(h->kernel_ent, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_ent, &te, &h->n_clusters_ent);
+      rc = plan_verify(h->kernel_ent, R, epv, C, h->smem, smem_bytes(R, true), &h->plan_ent, &h->n_clusters_ent);
     if (rc == SV_OK)
-      rc = plan_verify(h->kernel_lazy, R, epv, C, h->smem, smem_bytes(R, true), &h->smem_lazy, &tl, &h->n_clusters_lazy);
+      rc = plan_verify(h->kernel_lazy, R, epv, C, h->smem, smem_bytes(R, true), &h->plan_lazy, &h->n_clusters_lazy);
     if (rc != SV_OK) {
       cudaGetLastError();
       free_ctx(h);
