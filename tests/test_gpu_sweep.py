@@ -97,3 +97,42 @@ def test_sweep(lib, oracle, case):
         ok = np.isnan(r_h) | (np.abs(g_h - r_h) <= 2e-5 + 2e-6 * np.abs(r_h))
         assert ok.all(), float(np.nanmax(np.abs(g_h - r_h)))
     print(w.name, frac, stats)
+
+
+@pytest.mark.parametrize("T", [0.6, 1.0])
+def test_masked_warp_ranges(lib, oracle, T):
+    """Whole warp ranges of -inf in one row of a pair: at V = 151,552 bf16 a warp owns 2,304 or
+    2,560 consecutive logits of a CTA's 18,944, so a masked block of 6,000 covers at least one
+    range, whose part then has no reference.  Chains 0-3 mask the target row, 4-7 the draft row,
+    8-11 both, at every position (the bonus row too), in both the rounds whose exponentials wait
+    in tensor memory and the rounds that are recomputed."""
+    w = si.Workload(f"maskedwarps_T{T}", 12, 7, 151552, si.BF16, 2.0, draft_sigma=0.8, temp_lo=T, temp_hi=T)
+    b = si.generate(w)
+    neg_inf = np.uint16(0xFF80)
+    rng = np.random.default_rng(31)
+    for c in range(w.batch):
+        lo = int(rng.integers(0, 8)) * (w.vocab // 8) + int(rng.integers(0, 12000))
+        hi = lo + 6000
+        if c < 4 or c >= 8:
+            b.target[c, :, lo:hi] = neg_inf
+        if c >= 4:
+            b.draft[c, :, lo:hi] = neg_inf
+        inside = (b.tokens[c] >= lo) & (b.tokens[c] < hi)
+        b.tokens[c, inside] = (b.tokens[c, inside] + 7000) % w.vocab   # drafted tokens stay unmasked
+    ins = _dev(b)
+    v = lib.SpecVerifier(w.batch, w.k, w.vocab, torch.bfloat16)
+    full = v.verify(*ins, want_tv=True, want_entropy=True)
+    lazy = v.verify_lazy(*ins)
+    torch.cuda.synchronize()
+    rc, n_bad = v.get_error()
+    v.close()
+    got = {key: t.cpu().numpy() for key, t in full.items()}
+    ref = oracle.verify(b.target, b.draft, b.tokens, b.temperature, b.uniforms, w.dtype, nthreads=16)
+    assert int((ref["tau"] < 0).sum()) == 0 and n_bad == 0
+    _parity.assert_parity({key: got[key] for key in ("tokens", "tau", "p_draft", "q_draft", "tv")}, ref, w.k)
+    for key in ("tokens", "tau"):
+        assert np.array_equal(lazy[key].cpu().numpy(), got[key]), key
+    h_t, h_d = oracle.entropy_batch(b.target, b.draft, b.temperature, w.dtype, nthreads=16)
+    for g_h, r_h in ((got["entropy_target"], h_t), (got["entropy_draft"], h_d)):
+        g_h = g_h.astype(np.float64)
+        assert np.all(np.abs(g_h - r_h) <= 2e-5 + 2e-6 * np.abs(r_h)), float(np.max(np.abs(g_h - r_h)))
