@@ -423,6 +423,13 @@ __host__ __device__ constexpr int tmem_draft_rounds(int epv, int R) {
        : (256 / (R <= 10 ? 2 : 1) - epv * R) / epv;   // 256 / CTAs per SM = columns of warps 0..3
 }
 __host__ __device__ constexpr int tmem_cols_per_warp(int epv, int R) { return epv * (R + tmem_draft_rounds(epv, R)); }
+// Only instances whose allocation is 256 or 512 columns use TMEM (R >= 6 in
+// bf16, R >= 10 in fp32).  Their CTAs hold at least 86 registers per thread,
+// so the register file fits at most two of them on an SM, or one of 512
+// columns: whatever mix of this library's kernels shares an SM, its columns
+// never exceed 512 and no allocation waits on another of these kernels.  The
+// smaller instances (the smallest vocabularies) recompute in pass B instead.
+__host__ __device__ constexpr bool tmem_used(int epv, int R) { return 2 * tmem_cols_per_warp(epv, R) > 128; }
 template <int EPV, int R>
 __device__ __forceinline__ uint32_t tmem_warp_base(uint32_t base) {
   const uint32_t warp = threadIdx.x >> 5;
@@ -653,6 +660,8 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
                                              const uint32_t tm = 0) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
+  constexpr bool TM = tmem_used(EPV, R);   // exponentials kept in TMEM between the passes
+  constexpr int NS_T = TM ? R : 0, NS_D = TM ? tmem_draft_rounds(EPV, R) : 0;   // rounds kept per row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, V = P.V;
   const int b = un.b, ipos = un.ipos;
@@ -763,12 +772,12 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     const float rwt = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
     if constexpr (ENT) {   // the index fields carry sum e*a for sampling units
       float ea_t = 0.0f, ea_d = 0.0f;
-      if (PAIR) mine.s_t = rows_expsum_ent<Tl, R, R>(rt, cc, pk(-rwt, -rwt), last, ea_t, tm);
+      if (PAIR) mine.s_t = rows_expsum_ent<Tl, R, NS_T>(rt, cc, pk(-rwt, -rwt), last, ea_t, tm);
       else mine.s_t = rows_expsum_ent<Tl, R>(rt, cc, pk(-rwt, -rwt), last, ea_t);
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = rows_expsum_ent<Tl, R, tmem_draft_rounds(Lay<Tl>::EPV, R)>(rd, cc, pk(-rwd, -rwd), last, ea_d,
+        mine.s_d = rows_expsum_ent<Tl, R, NS_D>(rd, cc, pk(-rwd, -rwd), last, ea_d,
                                                                               tm + Lay<Tl>::EPV * R);
       }
       float v0 = mine.s_t, v1 = mine.s_d, v2 = ea_t, v3 = ea_d;
@@ -783,12 +792,12 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
     } else {
       // keep the target exponentials of a row pair in TMEM for pass B
-      mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R, R>(rt, cc, pk(-rwt, -rwt), last, tm)
+      mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R, NS_T>(rt, cc, pk(-rwt, -rwt), last, tm)
                                    : rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = warp_sum_f32(rows_expsum_store<Tl, R, tmem_draft_rounds(Lay<Tl>::EPV, R)>(
+        mine.s_d = warp_sum_f32(rows_expsum_store<Tl, R, NS_D>(
             rd, cc, pk(-rwd, -rwd), last, tm + Lay<Tl>::EPV * R));
       }
     }
@@ -939,9 +948,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   float wwarp;
   {
     // The target exponentials e_t = 2^(z_t c - ref_t) come back from TMEM
-    // (pass A stored them, relative to this warp's reference ref_t); the draft
-    // ones are recomputed relative to this warp's draft reference ref_d, as in
-    // pass A.  With s_t = 2^(ref_t - R_t) and s_d = 2^(ref_d - R_d) (exact
+    // (pass A stored them, relative to this warp's reference ref_t), as do the
+    // draft ones of the first rounds; the rest are recomputed relative to the
+    // warp's references, as in pass A (all of them in the instances without
+    // TMEM).  With s_t = 2^(ref_t - R_t) and s_d = 2^(ref_d - R_d) (exact
     // powers of 2), the weight on the row references is
     //   max(0, s_t e_t - r s_d e_d) = s_t * sat(e_t - r (s_d / s_t) e_d),
     // the clamp being exact because e_t <= 1; identical rows give exactly 0.
@@ -953,8 +963,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       const float nrs = mine.ref_d == NO_REF ? 0.0f : -M.r * sc;
       const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
       const u64 nrdw = pk(-rwd, -rwd);
-      tmem_wait_st();   // pass A's stores are complete
-      constexpr int ndr = tmem_draft_rounds(EPV, R);   // rounds whose draft exponentials were kept too
+      const float rwt = (float)mine.ref_t;
+      const u64 nrtw = pk(-rwt, -rwt);
+      if (TM) tmem_wait_st();   // pass A's stores are complete
+      constexpr int ndr = NS_D;   // rounds whose draft exponentials were kept too
       const uint32_t tmd = tm + EPV * R;
       u64 a0 = 0ull, a1 = 0ull;
       // one round: the weights of its EPV positions, from e_t and e_d (kept, or recomputed as in pass A)
@@ -986,14 +998,28 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
         if (j == R - 1 && !last) break;
         const bool kept = j < ndr;
         float et[EPV], ed[EPV];
-        if constexpr (EPV == 8) {
+        if constexpr (!TM) {   // recomputed as in pass A
+#pragma unroll
+          for (int q = 0; q < EPV / 2; ++q) {
+            float a0t, a1t;
+            if constexpr (EPV == 8) {
+              const uint32_t wt = q == 0 ? rt[j].x : q == 1 ? rt[j].y : q == 2 ? rt[j].z : rt[j].w;
+              upk(fma2(pk(bf_lo(wt), bf_hi(wt)), cc, nrtw), a0t, a1t);
+            } else {
+              const uint32_t wt0 = q == 0 ? rt[j].x : rt[j].z, wt1 = q == 0 ? rt[j].y : rt[j].w;
+              upk(fma2(pk(__uint_as_float(wt0), __uint_as_float(wt1)), cc, nrtw), a0t, a1t);
+            }
+            et[2 * q] = ex2(a0t);
+            et[2 * q + 1] = ex2(a1t);
+          }
+        } else if constexpr (EPV == 8) {
           tmem_ld8(tm + 8u * j, et);
           if (kept) tmem_ld8(tmd + 8u * j, ed);
         } else {
           tmem_ld4(tm + 4u * j, et);
           if (kept) tmem_ld4(tmd + 4u * j, ed);
         }
-        tmem_wait_ld();
+        if (TM) tmem_wait_ld();
         round_w(j, et, ed, kept);
       }
       float l, h;
@@ -1042,7 +1068,7 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
     S.cnt = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  constexpr bool USE_TMEM = true;   // target exponentials wait in TMEM from pass A to pass B
+  constexpr bool USE_TMEM = tmem_used(Lay<Tl>::EPV, R);   // exponentials wait in TMEM from pass A to pass B
   if (USE_TMEM && warp == 0) {   // the host keeps CTAs per SM x tmem_cols within the SM's 512 columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&S.tmem)),
                  "r"(P.tmem_cols) : "memory");
@@ -1854,12 +1880,23 @@ static int plan_verify(FusedFn f, int R, int epv, int C, size_t smem0, size_t sm
       cudaFuncGetAttributes(&fa, f) != cudaSuccess)
     return SV_ERR_CUDA;
   optin -= (int)fa.sharedSizeBytes;   // the limit covers dynamic shared memory only
-  int need = 32;   // warps 0..3 and 4..7 each take tmem_cols_per_warp columns
-  while (need < 2 * tmem_cols_per_warp(epv, R)) need <<= 1;
-  const int tmem_ctas = 512 / need;
+  const bool uses = tmem_used(epv, R);
+  int need = 0;   // warps 0..3 and 4..7 each take tmem_cols_per_warp columns
+  if (uses) {
+    need = 32;
+    while (need < 2 * tmem_cols_per_warp(epv, R)) need <<= 1;
+  }
+  const int tmem_ctas = uses ? 512 / need : 1 << 30;
   // registers are allocated per warp in multiples of 256
   const long long regs_cta = (long long)((fa.numRegs * 32 + 255) / 256 * 256) * (NT / 32);
   size_t sm = smem0;
+  // A TMEM instance must leave no room on an SM for a third such CTA of any
+  // of these kernels (a second one at 512 columns): by its registers, as
+  // every one compiled here does, or else by shared memory.
+  if (uses && regs_cta * (512 / need + 1) <= sm_regs) {
+    const size_t floor_smem = (size_t)(sm_smem / (512 / need + 1) - reserved - (int)fa.sharedSizeBytes + 1);
+    if (sm < floor_smem) sm = floor_smem;
+  }
   int ctas = 0;
   for (;;) {
     const long long by_smem = (long long)sm_smem / ((long long)sm + fa.sharedSizeBytes + reserved);
