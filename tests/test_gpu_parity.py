@@ -276,3 +276,35 @@ def test_staged_and_plain_handles_coexist(lib):
     assert staged.get_error() == (lib.SV_OK, 0) and plain.get_error() == (lib.SV_OK, 0)
     staged.close()
     plain.close()
+
+
+def test_concurrent_handles_on_streams(lib):
+    """Three handles whose kernels may share SMs, launched on three streams without waiting for
+    each other: V = 151,552 (256 tensor-memory columns per CTA), V = 262,144 (512 columns, one
+    CTA per SM) and V = 20,000 (no tensor memory).  Each result is bit-identical to the same
+    handle's result alone."""
+    ws = [si.C3_T1.scaled(batch=48), si.Workload("conc_v262144", 16, 7, 262144, si.BF16, 2.0, draft_sigma=0.8,
+                                                  temp_lo=1.0, temp_hi=1.0),
+          si.Workload("conc_v20000", 64, 7, 20000, si.BF16, 2.0, draft_sigma=0.8, temp_lo=0.7, temp_hi=0.7)]
+    handles, inputs, alone = [], [], []
+    for w in ws:
+        b = si.generate(w)
+        v = lib.SpecVerifier(w.batch, w.k, w.vocab, torch.bfloat16)
+        ins = to_dev(b)
+        out = v.verify(*ins, want_tv=True)
+        torch.cuda.synchronize()
+        handles.append(v); inputs.append(ins); alone.append({k: t.cpu().numpy() for k, t in out.items()})
+    streams = [torch.cuda.Stream() for _ in ws]
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for v, ins, s in zip(handles, inputs, streams):
+            outs.append(v.verify(*ins, want_tv=True, stream=s))
+    torch.cuda.synchronize()
+    for i, out in enumerate(outs):
+        ref = alone[i % len(ws)]
+        for key, t in out.items():
+            assert np.array_equal(t.cpu().numpy(), ref[key], equal_nan=True), (ws[i % len(ws)].name, key)
+    for v in handles:
+        assert v.get_error()[0] == 0
+        v.close()
