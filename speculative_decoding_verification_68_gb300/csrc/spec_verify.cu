@@ -503,8 +503,8 @@ __device__ __forceinline__ u64 clamp_m127(u64 x) {
   upk(x, lo, hi);
   return pk(fmaxf(lo, -127.0f), fmaxf(hi, -127.0f));
 }
-// (With STORE, every exponential also goes to this warp's TMEM columns, as in
-// rows_expsum_store.)
+// (The exponentials of rounds j < NSTORE also go to this warp's TMEM columns,
+// as in rows_expsum_store.)
 template <typename Tl, int R, int NSTORE = 0>
 __device__ __forceinline__ float rows_expsum_ent(const uint4 (&v)[R], u64 cc, u64 nr, bool last, float& ea,
                                                  uint32_t tm = 0) {
@@ -777,8 +777,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = rows_expsum_ent<Tl, R, NS_D>(rd, cc, pk(-rwd, -rwd), last, ea_d,
-                                                                              tm + Lay<Tl>::EPV * R);
+        mine.s_d = rows_expsum_ent<Tl, R, NS_D>(rd, cc, pk(-rwd, -rwd), last, ea_d, tm + EPV * R);
       }
       float v0 = mine.s_t, v1 = mine.s_d, v2 = ea_t, v3 = ea_d;
 #pragma unroll
@@ -791,14 +790,14 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       mine.s_t = v0; mine.s_d = v1;
       mine.i_t = __float_as_int(v2); mine.i_d = __float_as_int(v3);
     } else {
-      // keep the target exponentials of a row pair in TMEM for pass B
+      // a row pair keeps its target exponentials, and the draft ones of the first
+      // rounds, in TMEM for pass B (in the instances that use TMEM)
       mine.s_t = warp_sum_f32(PAIR ? rows_expsum_store<Tl, R, NS_T>(rt, cc, pk(-rwt, -rwt), last, tm)
                                    : rows_expsum<Tl, R>(rt, cc, pk(-rwt, -rwt), last));
       if (PAIR) {
         mine.ref_d = iref_of(mine.m_d, c);
         const float rwd = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
-        mine.s_d = warp_sum_f32(rows_expsum_store<Tl, R, NS_D>(
-            rd, cc, pk(-rwd, -rwd), last, tm + Lay<Tl>::EPV * R));
+        mine.s_d = warp_sum_f32(rows_expsum_store<Tl, R, NS_D>(rd, cc, pk(-rwd, -rwd), last, tm + EPV * R));
       }
     }
   }
@@ -1787,10 +1786,10 @@ void pick_kernels(int r, FusedFn& f, FusedFn& fe, FusedFn& fl, FinalFn& g) {
 }  // namespace
 
 // ------------------------------------------------------------------ host side
-// launch plan of one TMEM-using verification instance
+// launch plan of one verification instance
 struct VerifyPlan {
   size_t smem;        // dynamic shared memory (padded above the staged size when TMEM columns need it)
-  int tmem_cols;      // TMEM columns per CTA
+  int tmem_cols;      // TMEM columns per CTA (0: the instance uses none)
 };
 
 struct spec_verify_ctx {
