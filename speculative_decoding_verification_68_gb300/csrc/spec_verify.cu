@@ -827,16 +827,18 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       ia = lane < g.items() ? S.x1[set1][lane] : z;
       ib = lane + 32 < g.items() ? S.x1[set1][lane + 32] : z;
     }
-    const float M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
-    const float M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
+    float M_t, M_d;
     int A_t = 0, A_d = 0, IR_t = NO_REF, IR_d = NO_REF;
     float S_t = 0.0f, S_d = 0.0f;
     if (greedy) {
+      M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+      M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
       A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
       if (PAIR)
         A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
     } else {
-      // the row reference is the largest item reference (ceil is monotonic)
+      // the row reference is the largest item reference (ceil is monotonic);
+      // the maxima, needed only for the status, are reduced after the sums
       IR_t = warp_max_s32(max(ia.ref_t, ib.ref_t));
       if (PAIR) {
         IR_d = warp_max_s32(max(ia.ref_d, ib.ref_d));
@@ -851,6 +853,8 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       } else {
         S_t = warp_sum_f32(ia.s_t * pow2_diff(ia.ref_t, IR_t) + ib.s_t * pow2_diff(ib.ref_t, IR_t));
       }
+      M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+      M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
     }
     const float R_t = IR_t == NO_REF ? 0.0f : (float)IR_t, R_d = IR_d == NO_REF ? 0.0f : (float)IR_d;
     bool row_ok = isfinite(M_t) && (!PAIR || isfinite(M_d));
@@ -889,6 +893,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
         if (PAIR) P.out_ent_d[pi] = H_d;
       }
     }
+    Merged m;
     if (lane == 0) {
       int cont = 0;   // the same test as the accept test below, on the same values
       if (LAZY && PAIR && status == 0) {
@@ -899,10 +904,15 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
           cont = S.gz_u < exp2f(lpx - lqx) * (S_d / S_t);
         }
       }
-      Merged m;
       m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
       m.grab = LAZY && carry ? S.grab[set1] : -1;
       mg = m;
+    }
+    __syncwarp();
+    merged_arrive();
+    // rank 0's workspace writes come after the other warps are released: only
+    // the finalize kernel reads them
+    if (lane == 0) {
       if (g.rank() == 0) {
         UnitStat st;
         st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
@@ -920,12 +930,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
           if (LAZY && PAIR && status != 0) P.ws_acc[pi] = 0;   // an invalid position stops the chain
           if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
         } else if (LAZY && PAIR) {
-          P.ws_acc[pi] = cont;
+          P.ws_acc[pi] = m.cont;
         }
       }
     }
-    __syncwarp();
-    merged_arrive();
   } else {
     merged_wait();
   }
