@@ -187,6 +187,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t a, unsigned parity) {
 // Bounded wait for a stage: gives up (and flags the handle) instead of hanging.
 // Once any wait has given up, the others see the flag and return within 256 polls.
 constexpr int WAIT_POLLS = 1 << 18;   // about 1 s: a poll suspends for ~3.8 us on GB300
+// A 4-byte asynchronous copy from global to shared memory, and the wait for
+// this thread's copies.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void mbar_wait_bounded(uint32_t a, unsigned parity, int* flags, int polls = WAIT_POLLS) {
   for (int it = 0; it < polls; ++it) {
     if (mbar_try(a, parity)) return;
@@ -650,6 +656,22 @@ __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, 
 __device__ __forceinline__ void merged_arrive() { asm volatile("bar.arrive 1, %0;" ::"n"(NT) : "memory"); }
 __device__ __forceinline__ void merged_wait() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
+// A warp's residual mass of its range whose lane sum is still to be taken: the
+// five shuffle steps run during the next unit's copy, where they overlap the
+// shared-memory loads, instead of at the end of pass B.
+struct PendingMass {
+  float w;        // this lane's part
+  size_t item;    // the range's slot in ws_w
+  bool on;
+};
+__device__ __forceinline__ void flush_mass(const KParams& P, PendingMass* pm) {
+  if (pm && pm->on) {
+    const float w = warp_sum_f32(pm->w);
+    if ((threadIdx.x & 31) == 0) P.ws_w[pm->item] = w;
+    pm->on = false;
+  }
+}
+
 // Returns, for lazy verification, whether the chain goes on to its next
 // position (the same in every CTA of the cluster); 0 otherwise.
 template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
@@ -657,7 +679,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
                                              const float T, const int x, const bool carry = false,
-                                             const uint32_t tm = 0) {
+                                             const uint32_t tm = 0, PendingMass* pm = nullptr) {
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   constexpr bool TM = tmem_used(EPV, R);   // exponentials kept in TMEM between the passes
@@ -699,7 +721,9 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       const unsigned char* bd = smem_stage + ((size_t)(1 * NWARP + wb) * R * 32 + iv) * 16;
       S.gz_t = Lay<Tl>::load_scalar(bt, lx % EPV);
       S.gz_d = Lay<Tl>::load_scalar(bd, lx % EPV);
+      cp_async4(&S.gz_u, P.uniforms + (size_t)b * (k + 1) + ipos);   // for the accept test, which ends the unit
     }
+    flush_mass(P, pm);   // the previous unit's residual mass, while the loads land
     __syncwarp();
     bool last = false;
     if (lane == 0) last = stage_release_last(&S.cnt);
@@ -725,7 +749,9 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     if (PAIR && tid == 0 && own_x) {
       S.gz_t = Lay<Tl>::load_scalar(P.target, trow * V + x);
       S.gz_d = Lay<Tl>::load_scalar(P.draft, drow * V + x);
+      cp_async4(&S.gz_u, P.uniforms + (size_t)b * (k + 1) + ipos);
     }
+    flush_mass(P, pm);
   }
 
   if (LAZY && PAIR && tid == 0) {   // parked in shared memory, out of the registers pass A needs
@@ -863,7 +889,9 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
     }
     const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
-    const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;   // q_j = e_d * r / S_t
+    // q_j = e_d * r / S_t.  The fast quotient is well inside the tolerance; equal
+    // sums take r = 1 exactly, so identical rows keep an exactly zero residual.
+    const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;
     if constexpr (ENT) {
       // Row entropies.  Each item's sum e*a is relative to its own reference;
       // on the row reference it becomes 2^(ref_i - R) * (EA_i + (ref_i - R) * s_i).
@@ -939,7 +967,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   }
   const Merged M = mg;
   // cluster-uniform; an accepted position of a lazy walk needs no residual
-  if (M.status != 0 || greedy || (LAZY && M.cont)) return M.cont;
+  if (M.status != 0 || greedy || (LAZY && M.cont)) {
+    if (!LAZY && own_x && tid == 0) cp_async_wait_all();   // no accept test: the copied uniform is not used
+    return M.cont;
+  }
 
   // this range's part of S_t (the target mass, and the draw from p when the residual is zero)
   const float pmass = mine.s_t * pow2_diff(mine.ref_t, M.IR_t);
@@ -952,7 +983,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
 
   // ---------------- pass B: residual mass of this warp's range
   const u64 cc = pk(c, c);
-  float wwarp;
+  float wacc = 0.0f;
   {
     // The target exponentials e_t = 2^(z_t c - ref_t) come back from TMEM
     // (pass A stored them, relative to this warp's reference ref_t), as do the
@@ -962,7 +993,6 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     // powers of 2), the weight on the row references is
     //   max(0, s_t e_t - r s_d e_d) = s_t * sat(e_t - r (s_d / s_t) e_d),
     // the clamp being exact because e_t <= 1; identical rows give exactly 0.
-    float wacc = 0.0f;
     if (mine.ref_t != NO_REF) {   // else the warp's target range is all masked: no residual
       constexpr int EPV = Lay<Tl>::EPV;
       const int e_sc = mine.ref_d == NO_REF ? 0 : (mine.ref_d - (int)M.R_d) - (mine.ref_t - M.IR_t);
@@ -1033,13 +1063,20 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       upk(add2(a0, a1), l, h);
       wacc = (l + h) * pow2_diff(mine.ref_t, M.IR_t);
     }
-    wwarp = warp_sum_f32(wacc);
   }
-  if (lane == 0) P.ws_w[item] = wwarp;
+  if (pm) {   // summed over the lanes during the next unit's copy (or after the last unit)
+    pm->w = wacc;
+    pm->item = item;
+    pm->on = true;
+  } else {
+    const float wwarp = warp_sum_f32(wacc);
+    if (lane == 0) P.ws_w[item] = wwarp;
+  }
   if (!LAZY && own_x && tid == 0) {   // accept test at the drafted token
     const float lpx = fmaf(S.gz_t, c, -M.R_t), lqx = fmaf(S.gz_d, c, -M.R_d);
     const float ratio = exp2f(lpx - lqx) * (M.S_d / M.S_t);
-    const float u_acc = P.uniforms[(size_t)b * (k + 1) + ipos];
+    cp_async_wait_all();   // the uniform copied in at the start of the unit
+    const float u_acc = S.gz_u;
     P.ws_acc[pi] = u_acc < ratio ? 1 : 0;
     if (P.out_p) P.out_p[pi] = exp2f(lpx) / M.S_t;
     if (P.out_q) P.out_q[pi] = exp2f(lqx) / M.S_d;
@@ -1148,6 +1185,8 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
     unsigned u = cid;
     Unit cur = unit_of(u, B);
     if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+    PendingMass pm;
+    pm.on = false;
     for (; u < n_units; u += ncl, phase ^= 1u) {
       const bool has_next = u + ncl < n_units;
       const Unit next = unit_of(u + ncl, B);
@@ -1156,12 +1195,13 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
       const bool tma_next = P.tma && has_next;
       if (cur.ipos < k)
         process_unit<Tl, R, true, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
-                                              false, tm);
+                                              false, tm, &pm);
       else
         process_unit<Tl, R, false, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
-                                               false, tm);
+                                               false, tm, &pm);
       cur = next;
     }
+    flush_mass(P, &pm);
   }
   if (USE_TMEM) {   // every TMEM access of the CTA is complete before its columns are freed
     tmem_wait_st();
