@@ -889,8 +889,8 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
     }
     const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
-    // q_j = e_d * r / S_t.  The fast quotient is well inside the tolerance; equal
-    // sums take r = 1 exactly, so identical rows keep an exactly zero residual.
+    // q_j = e_d * r / S_t, correctly rounded: equal sums give r = 1 exactly, so
+    // identical rows keep an exactly zero residual.
     const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;
     if constexpr (ENT) {
       // Row entropies.  Each item's sum e*a is relative to its own reference;
