@@ -39,7 +39,11 @@
  *     by spec_verify_get_error, which synchronises.
  *   - Argument errors are detected on the host before any launch and
  *     returned as a status; no exception crosses the interface.
- *   - A handle is not thread-safe; use one handle per stream.
+ *   - A handle is not thread-safe; use one handle per stream.  Different
+ *     handles may run at the same time on different streams: their kernels
+ *     can share SMs, and the tensor memory they allocate per CTA (256 or 512
+ *     columns, in the larger instances) never exceeds an SM's 512 columns
+ *     whatever the mix, so no launch waits on another.
  *   - Uniforms are in [0, 1); the seeded generator used by this project
  *     produces them on the 2^-24 lattice.
  *   - Limits: 1 <= k <= 31; V <= 327680 (bf16) or 163840 (fp32).  Above
