@@ -892,9 +892,28 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     // q_j = e_d * r / S_t, correctly rounded: equal sums give r = 1 exactly, so
     // identical rows keep an exactly zero residual.
     const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;
-    if constexpr (ENT) {
-      // Row entropies.  Each item's sum e*a is relative to its own reference;
-      // on the row reference it becomes 2^(ref_i - R) * (EA_i + (ref_i - R) * s_i).
+    Merged m;
+    if (lane == 0) {
+      int cont = 0;   // the same test as the accept test below, on the same values
+      if (LAZY && PAIR && status == 0) {
+        if (greedy) {
+          cont = x == A_t;
+        } else {
+          const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
+          cont = S.gz_u < exp2f(lpx - lqx) * (S_d / S_t);
+        }
+      }
+      m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
+      m.grab = LAZY && carry ? S.grab[set1] : -1;
+      mg = m;
+    }
+    __syncwarp();
+    merged_arrive();
+    if (ENT && g.rank() == 0) {
+      // Row entropies, by rank 0 alone (the only CTA that writes them) and
+      // after the other warps are released.  Each item's sum e*a is relative
+      // to its own reference; on the row reference it becomes
+      // 2^(ref_i - R) * (EA_i + (ref_i - R) * s_i).
       float H_t = __int_as_float(0x7fc00000), H_d = H_t;
       if (greedy) {   // the one-hot greedy distribution (NaN for an invalid temperature)
         if (t_ok && isfinite(M_t)) H_t = 0.0f;
@@ -916,28 +935,11 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
         if (ok_t) H_t = row_entropy(S_t, e_t);
         if (PAIR && ok_d) H_d = row_entropy(S_d, e_d);
       }
-      if (lane == 0 && g.rank() == 0) {
+      if (lane == 0) {
         P.out_ent_t[ui] = H_t;
         if (PAIR) P.out_ent_d[pi] = H_d;
       }
     }
-    Merged m;
-    if (lane == 0) {
-      int cont = 0;   // the same test as the accept test below, on the same values
-      if (LAZY && PAIR && status == 0) {
-        if (greedy) {
-          cont = x == A_t;
-        } else {
-          const float lpx = fmaf(S.gz_t, c, -R_t), lqx = fmaf(S.gz_d, c, -R_d);
-          cont = S.gz_u < exp2f(lpx - lqx) * (S_d / S_t);
-        }
-      }
-      m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
-      m.grab = LAZY && carry ? S.grab[set1] : -1;
-      mg = m;
-    }
-    __syncwarp();
-    merged_arrive();
     // rank 0's workspace writes come after the other warps are released: only
     // the finalize kernel reads them
     if (lane == 0) {
