@@ -107,7 +107,9 @@ int spec_verify_init(spec_verify_t* h, int max_batch, int k, int vocab, int logi
  *                               token, then -1 padding
  *   out_tau        [batch]      int32: accepted drafts 0..k (-1: invalid chain)
  *   out_p_draft    [batch, k]   fp32 or NULL: p_i(x_i) for every position
- *   out_q_draft    [batch, k]   fp32 or NULL: q_i(x_i) for every position
+ *                               (NaN where the position's rows, temperature
+ *                               or token are invalid)
+ *   out_q_draft    [batch, k]   fp32 or NULL: q_i(x_i) for every position (same)
  *   out_tv         [batch, k]   fp32 or NULL: TV distance of every position
  * Integer and fp32 arrays must be 4-byte aligned; logits whose base is
  * 16-byte aligned and whose row size V*sizeof(elem) is a multiple of 16 use

@@ -130,6 +130,8 @@ struct alignas(16) Merged {
   int status;          // ST_* bits, 0 if valid
   int cont;            // lazy verification: the chain goes on to the next position
   int grab;            // lazy verification: the counter value rank 0 drew for this unit (-1: none)
+  int IR_d;            // a bonus pair: the second row's integer reference (NO_REF as for IR_t)
+  int status_d;        // a bonus pair: the second row's ST_* bits
 };
 
 struct Small {
@@ -605,13 +607,36 @@ struct Geo {
   __device__ __forceinline__ int rounds() const { return warp_rounds((int)(threadIdx.x >> 5), p->rbase, p->rextra); }
 };
 
-// Units are taken position-major, u = ipos * B + b, so that every cluster's
-// walk u = cluster_id, cluster_id + n_clusters, ... meets every position
-// (and the cheaper bonus rows) equally often.
+// Units are taken position-major, u = ipos * B + b for the k verified
+// positions, so that every cluster's walk u = cluster_id, cluster_id +
+// n_clusters, ... meets every position equally often.  The bonus rows follow.
+// With PAIRED (instances of two CTAs per SM) they go two chains to a unit
+// (chains b = 2j and b + 1; the last one alone when B is odd): a bonus row
+// needs only its row statistics, so a pair of them fills the stage as a row
+// pair does and takes one exchange and one merge instead of two.  The pair's
+// second row is read after the first (the registers hold one row), so the
+// stage is released later; at one CTA per SM nothing hides the next unit's
+// copy behind that, and those instances take the bonus rows one at a time.
 struct Unit {
   int b, ipos;
 };
-__device__ __forceinline__ Unit unit_of(unsigned u, unsigned B) {
+template <bool PAIRED>
+__device__ __forceinline__ Unit unit_of(unsigned u, unsigned B, unsigned k) {
+  Unit r;
+  if (u < B * k) {
+    const unsigned ipos = u / B;
+    r.b = (int)(u - ipos * B);
+    r.ipos = (int)ipos;
+  } else {
+    r.b = (int)((PAIRED ? 2u : 1u) * (u - B * k));
+    r.ipos = (int)k;
+  }
+  return r;
+}
+// Instances whose verification walk pairs the bonus rows.
+template <int R> __host__ __device__ constexpr bool pairs_bonus_rows() { return R <= 10; }
+// The same for a walk over the k verified positions alone.
+__device__ __forceinline__ Unit pos_unit_of(unsigned u, unsigned B) {
   const unsigned ipos = u / B;
   Unit r;
   r.b = (int)(u - ipos * B);
@@ -621,30 +646,52 @@ __device__ __forceinline__ Unit unit_of(unsigned u, unsigned B) {
 
 template <typename Tl> __device__ __forceinline__ int nvec_of(const Geo& g) { return (g.slen() + Lay<Tl>::EPV - 1) / Lay<Tl>::EPV; }
 
+// Lowest global index in this warp's range of a row that holds the warp's
+// maximum m (greedy rows).
+template <typename Tl, int R>
+__device__ __forceinline__ int warp_argmax(const uint4 (&r)[R], float m, const Geo& g) {
+  constexpr int EPV = Lay<Tl>::EPV;
+  const int lane = threadIdx.x & 31;
+  int ci = 0x7fffffff;
+#pragma unroll
+  for (int j = R - 1; j >= 0; --j) {
+#pragma unroll
+    for (int e = EPV - 1; e >= 0; --e) {
+      const int gi = (int)g.slice0() + (g.vbeg() + j * 32 + lane) * EPV + e;
+      if (Lay<Tl>::elem(r[j], e) == m) ci = gi;
+    }
+  }
+  return (int)warp_min_u32((unsigned)ci);
+}
+
 // Bulk copies of one unit into the warp blocks of the stage, issued by one
 // whole warp: lane 0 arms the mbarrier with the byte count, then lane w
 // copies warp w's range of the target row and lane 8 + w that of the draft row.
-template <typename Tl, int R>
+// With BONUS_PAIRS (the verification walk), a bonus unit of chain b < B - 1
+// copies the bonus row of chain b + 1 in place of the draft row.
+template <typename Tl, int R, bool BONUS_PAIRS = false>
 __device__ __forceinline__ void issue_unit_load(const KParams& P, const Geo& g, Unit n, uint32_t bar,
                                                 const unsigned char* stage) {
   constexpr int ES = (int)sizeof(Tl);
   const int lane = threadIdx.x & 31;
   const int k = P.k;
   const bool pair = n.ipos < k;
+  const bool two = pair || (BONUS_PAIRS && n.b + 1 < P.B);   // two rows in the stage
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic accesses of the stage first
-  const long long trow = (long long)n.b * (k + 1) + n.ipos, drow = (long long)n.b * k + n.ipos;
+  const long long trow = (long long)n.b * (k + 1) + n.ipos;
+  const long long drow = BONUS_PAIRS && !pair ? (long long)(n.b + 1) * (k + 1) + k : (long long)n.b * k + n.ipos;
   if (lane == 0) {
     const unsigned bytes = (unsigned)nvec_of<Tl>(g) * 16u;
-    if (bytes > 0) mbar_expect_tx(bar, pair ? 2 * bytes : bytes);
+    if (bytes > 0) mbar_expect_tx(bar, two ? 2 * bytes : bytes);
     else mbar_arrive(bar);
   }
   __syncwarp();
   const int w = lane & 7, row = lane >> 3;
-  if (lane < 16 && (row == 0 || pair)) {
+  if (lane < 16 && (row == 0 || two)) {
     const int vb = warp_vbeg(w, P.rbase, P.rextra);
     const int len = max(0, min(32 * warp_rounds(w, P.rbase, P.rextra), nvec_of<Tl>(g) - vb));
     if (len > 0) {
-      const char* src = (const char*)(row == 0 ? P.target : P.draft) +
+      const char* src = (const char*)(row == 0 || (BONUS_PAIRS && !pair) ? P.target : P.draft) +
                         ((size_t)(row == 0 ? trow : drow) * P.V + g.slice0()) * ES + (size_t)vb * 16;
       const uint32_t dst = saddr(stage + ((size_t)(row * NWARP + w) * R * 32) * 16);
       bulk_g2s(dst, src, (unsigned)len * 16u, bar);
@@ -672,14 +719,22 @@ __device__ __forceinline__ void flush_mass(const KParams& P, PendingMass* pm) {
   }
 }
 
+// Unit kinds: a verified position (the target and draft rows of one chain),
+// one bonus row, or the bonus rows of two chains (the second one, of chain
+// un.b + 1 at temperature T2, in the draft slots).
+enum { U_BONUS = 0, U_PAIR = 1, U_BONUS2 = 2 };
+
 // Returns, for lazy verification, whether the chain goes on to its next
 // position (the same in every CTA of the cluster); 0 otherwise.
-template <typename Tl, int R, bool PAIR, bool ENT, bool LAZY>
+template <typename Tl, int R, int KIND, bool ENT, bool LAZY>
 __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const uint4* blk_t, const uint4* blk_d,
                                              const Geo& g, const Unit un, unsigned phase, int& n1, const uint32_t bar,
                                              const unsigned char* smem_stage, const Unit next, bool tma_next,
                                              const float T, const int x, const bool carry = false,
-                                             const uint32_t tm = 0, PendingMass* pm = nullptr) {
+                                             const uint32_t tm = 0, PendingMass* pm = nullptr, const float T2 = 0.0f) {
+  constexpr bool PAIR = KIND == U_PAIR;     // a verified position
+  constexpr bool B2 = KIND == U_BONUS2;     // two bonus rows
+  static_assert(!(B2 && LAZY), "the lazy walk takes bonus rows one at a time");
   constexpr int EPV = Lay<Tl>::EPV;
   constexpr int ES = (int)sizeof(Tl);
   constexpr bool TM = tmem_used(EPV, R);   // exponentials kept in TMEM between the passes
@@ -705,6 +760,14 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   uint4 rt[R], rd[R];
   bool own_x = false;
   const bool last = g.rounds() == R;   // warp-uniform: this warp owns a last round
+  // This warp is done with the stage; the last warp to finish issues the next unit's copy.
+  auto release_stage = [&]() {
+    __syncwarp();
+    bool fin = false;
+    if (lane == 0) fin = stage_release_last(&S.cnt);
+    fin = __shfl_sync(FULL, fin, 0);
+    if (fin && tma_next) issue_unit_load<Tl, R, !LAZY && pairs_bonus_rows<R>()>(P, g, next, bar, smem_stage);
+  };
   if (P.tma) {
     mbar_wait_bounded(bar, phase, P.flags);
 #pragma unroll
@@ -724,11 +787,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       cp_async4(&S.gz_u, P.uniforms + (size_t)b * (k + 1) + ipos);   // for the accept test, which ends the unit
     }
     flush_mass(P, pm);   // the previous unit's residual mass, while the loads land
-    __syncwarp();
-    bool last = false;
-    if (lane == 0) last = stage_release_last(&S.cnt);
-    last = __shfl_sync(FULL, last, 0);
-    if (last && tma_next) issue_unit_load<Tl, R>(P, g, next, bar, smem_stage);
+    if (!B2) release_stage();   // a bonus pair still needs its second row from the stage
   } else {
     const long long trow = (long long)b * (k + 1) + ipos, drow = (long long)b * k + ipos;
     const char* tb = (const char*)P.target + ((size_t)trow * V + g.slice0()) * ES;
@@ -764,6 +823,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   const bool greedy = !(T > 0.0f) || !t_ok;      // invalid temperatures take the cheap path
   const bool x_ok = !PAIR || P.tv_only || (x >= 0 && x < V);
   const float c = greedy ? 0.0f : fminf(__fdiv_rn(LOG2E_F, T), 3.0e38f);
+  // a bonus pair: the second chain's temperature, taken the same way
+  const bool t_ok2 = T2 >= 0.0f && T2 <= 3.0e38f;
+  const bool greedy2 = !(T2 > 0.0f) || !t_ok2;
+  const float c2 = greedy2 ? 0.0f : fminf(__fdiv_rn(LOG2E_F, T2), 3.0e38f);
 
   // ---------------- pass A: per-warp statistics, pushed to every CTA of the cluster
   MaxAcc<Tl> mx_t, mx_d;
@@ -779,7 +842,63 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
   mine.i_t = 0x7fffffff; mine.i_d = 0x7fffffff;
   mine.s_t = 0.0f; mine.s_d = 0.0f;
   mine.ref_t = NO_REF; mine.ref_d = NO_REF;
-  if (greedy) {
+  if constexpr (B2) {
+    // Each row as a lone bonus row would take it, with its chain's temperature;
+    // the second row comes into the registers once the first is done with them.
+    float s_t = 0.0f, s_d = 0.0f, ea_t = 0.0f, ea_d = 0.0f;
+    if (greedy) {
+      mine.i_t = warp_argmax<Tl, R>(rt, mine.m_t, g);
+    } else {
+      mine.ref_t = iref_of(mine.m_t, c);
+      const float rw = mine.ref_t == NO_REF ? 0.0f : (float)mine.ref_t;
+      if constexpr (ENT) s_t = rows_expsum_ent<Tl, R>(rt, pk(c, c), pk(-rw, -rw), last, ea_t);
+      else mine.s_t = warp_sum_f32(rows_expsum<Tl, R>(rt, pk(c, c), pk(-rw, -rw), last));
+    }
+    if (P.tma) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) rd[j] = j < R - 1 || last ? blk_d[j * 32 + lane] : Lay<Tl>::neg_inf();
+      release_stage();
+    } else {
+      const char* db = (const char*)P.target + ((size_t)((long long)(b + 1) * (k + 1) + ipos) * V + g.slice0()) * ES;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int v = g.vbeg() + j * 32 + lane;
+        const bool in = j < g.rounds() && v < nvec_of<Tl>(g);
+        rd[j] = P.vec16 ? (in ? __ldg(reinterpret_cast<const uint4*>(db) + v) : Lay<Tl>::neg_inf())
+                        : load_vec_direct<Tl>(db, v, g.slen(), in);
+      }
+    }
+    {
+      MaxAcc<Tl> mx2;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (j == R - 1 && !last) break;
+        mx2.add(rd[j]);
+      }
+      mine.m_d = warp_max_nan(mx2.get());
+    }
+    if (greedy2) {
+      mine.i_d = warp_argmax<Tl, R>(rd, mine.m_d, g);
+    } else {
+      mine.ref_d = iref_of(mine.m_d, c2);
+      const float rw = mine.ref_d == NO_REF ? 0.0f : (float)mine.ref_d;
+      if constexpr (ENT) s_d = rows_expsum_ent<Tl, R>(rd, pk(c2, c2), pk(-rw, -rw), last, ea_d);
+      else mine.s_d = warp_sum_f32(rows_expsum<Tl, R>(rd, pk(c2, c2), pk(-rw, -rw), last));
+    }
+    if constexpr (ENT) {   // the index fields carry sum e*a for sampling rows
+      if (!greedy || !greedy2) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float y0 = __shfl_xor_sync(FULL, s_t, o), y1 = __shfl_xor_sync(FULL, s_d, o);
+          const float y2 = __shfl_xor_sync(FULL, ea_t, o), y3 = __shfl_xor_sync(FULL, ea_d, o);
+          upk(add2(pk(s_t, s_d), pk(y0, y1)), s_t, s_d);
+          upk(add2(pk(ea_t, ea_d), pk(y2, y3)), ea_t, ea_d);
+        }
+      }
+      if (!greedy) { mine.s_t = s_t; mine.i_t = __float_as_int(ea_t); }
+      if (!greedy2) { mine.s_d = s_d; mine.i_d = __float_as_int(ea_d); }
+    }
+  } else if (greedy) {
     int ci_t = 0x7fffffff, ci_d = 0x7fffffff;   // lowest global index holding the warp maximum
 #pragma unroll
     for (int j = R - 1; j >= 0; --j) {
@@ -856,7 +975,24 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     float M_t, M_d;
     int A_t = 0, A_d = 0, IR_t = NO_REF, IR_d = NO_REF;
     float S_t = 0.0f, S_d = 0.0f;
-    if (greedy) {
+    if constexpr (B2) {   // two independent rows, each merged as a lone bonus row is
+      if (greedy) {
+        M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+        A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
+      } else {
+        IR_t = warp_max_s32(max(ia.ref_t, ib.ref_t));
+        S_t = warp_sum_f32(ia.s_t * pow2_diff(ia.ref_t, IR_t) + ib.s_t * pow2_diff(ib.ref_t, IR_t));
+        M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
+      }
+      if (greedy2) {
+        M_d = warp_max_nan(nanmax(ia.m_d, ib.m_d));
+        A_d = (int)warp_min_u32((unsigned)min(ia.m_d == M_d ? ia.i_d : 0x7fffffff, ib.m_d == M_d ? ib.i_d : 0x7fffffff));
+      } else {
+        IR_d = warp_max_s32(max(ia.ref_d, ib.ref_d));
+        S_d = warp_sum_f32(ia.s_d * pow2_diff(ia.ref_d, IR_d) + ib.s_d * pow2_diff(ib.ref_d, IR_d));
+        M_d = warp_max_nan(nanmax(ia.m_d, ib.m_d));
+      }
+    } else if (greedy) {
       M_t = warp_max_nan(nanmax(ia.m_t, ib.m_t));
       M_d = PAIR ? warp_max_nan(nanmax(ia.m_d, ib.m_d)) : 0.0f;
       A_t = (int)warp_min_u32((unsigned)min(ia.m_t == M_t ? ia.i_t : 0x7fffffff, ib.m_t == M_t ? ib.i_t : 0x7fffffff));
@@ -889,6 +1025,12 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       if (PAIR) row_ok = row_ok && fabsf(M_d * c) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
     }
     const int status = (t_ok ? 0 : ST_TEMP) | (x_ok ? 0 : ST_TOKEN) | (row_ok ? 0 : ST_ROW);
+    int status_d = 0;   // a bonus pair: the second row's status, taken the same way
+    if constexpr (B2) {
+      bool ok2 = isfinite(M_d);
+      if (!greedy2) ok2 = ok2 && fabsf(M_d * c2) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
+      status_d = (t_ok2 ? 0 : ST_TEMP) | (ok2 ? 0 : ST_ROW);
+    }
     // q_j = e_d * r / S_t, correctly rounded: equal sums give r = 1 exactly, so
     // identical rows keep an exactly zero residual.
     const float r_f = PAIR && !greedy ? S_t / S_d : 0.0f;
@@ -905,6 +1047,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       }
       m.S_t = S_t; m.S_d = S_d; m.R_t = R_t; m.R_d = R_d; m.r = r_f; m.IR_t = IR_t; m.status = status; m.cont = cont;
       m.grab = LAZY && carry ? S.grab[set1] : -1;
+      m.IR_d = IR_d; m.status_d = status_d;
       mg = m;
     }
     __syncwarp();
@@ -915,13 +1058,29 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       // to its own reference; on the row reference it becomes
       // 2^(ref_i - R) * (EA_i + (ref_i - R) * s_i).
       float H_t = __int_as_float(0x7fc00000), H_d = H_t;
-      if (greedy) {   // the one-hot greedy distribution (NaN for an invalid temperature)
+      auto part = [&](float s_i, float ea_i, int ref_i, int IR) {   // empty ranges and padding add 0
+        return ref_i == NO_REF ? 0.0f : pow2_diff(ref_i, IR) * fmaf((float)ref_i - (float)IR, s_i, ea_i);
+      };
+      if constexpr (B2) {   // each row with its own temperature
+        if (greedy && t_ok && isfinite(M_t)) H_t = 0.0f;
+        if (greedy2 && t_ok2 && isfinite(M_d)) H_d = 0.0f;
+        if (!greedy || !greedy2) {
+          float e_t = part(ia.s_t, __int_as_float(ia.i_t), ia.ref_t, IR_t) + part(ib.s_t, __int_as_float(ib.i_t), ib.ref_t, IR_t);
+          float e_d = part(ia.s_d, __int_as_float(ia.i_d), ia.ref_d, IR_d) + part(ib.s_d, __int_as_float(ib.i_d), ib.ref_d, IR_d);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float y0 = __shfl_xor_sync(FULL, e_t, o), y1 = __shfl_xor_sync(FULL, e_d, o);
+            upk(add2(pk(e_t, e_d), pk(y0, y1)), e_t, e_d);
+          }
+          const bool ok_t = t_ok && isfinite(M_t) && fabsf(M_t * c) < REF_LIMIT && S_t > 0.0f && isfinite(S_t);
+          const bool ok_d = t_ok2 && isfinite(M_d) && fabsf(M_d * c2) < REF_LIMIT && S_d > 0.0f && isfinite(S_d);
+          if (!greedy && ok_t) H_t = row_entropy(S_t, e_t);
+          if (!greedy2 && ok_d) H_d = row_entropy(S_d, e_d);
+        }
+      } else if (greedy) {   // the one-hot greedy distribution (NaN for an invalid temperature)
         if (t_ok && isfinite(M_t)) H_t = 0.0f;
         if (t_ok && PAIR && isfinite(M_d)) H_d = 0.0f;
       } else {
-        auto part = [&](float s_i, float ea_i, int ref_i, int IR) {   // empty ranges and padding add 0
-          return ref_i == NO_REF ? 0.0f : pow2_diff(ref_i, IR) * fmaf((float)ref_i - (float)IR, s_i, ea_i);
-        };
         float e_t = part(ia.s_t, __int_as_float(ia.i_t), ia.ref_t, IR_t) + part(ib.s_t, __int_as_float(ib.i_t), ib.ref_t, IR_t);
         float e_d = PAIR ? part(ia.s_d, __int_as_float(ia.i_d), ia.ref_d, IR_d) + part(ib.s_d, __int_as_float(ib.i_d), ib.ref_d, IR_d)
                          : 0.0f;
@@ -938,6 +1097,7 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
       if (lane == 0) {
         P.out_ent_t[ui] = H_t;
         if (PAIR) P.out_ent_d[pi] = H_d;
+        if (B2) P.out_ent_t[(size_t)(b + 1) * (k + 1) + ipos] = H_d;
       }
     }
     // rank 0's workspace writes come after the other warps are released: only
@@ -945,9 +1105,17 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     if (lane == 0) {
       if (g.rank() == 0) {
         UnitStat st;
-        st.c = c; st.R_t = R_t; st.R_d = R_d; st.r = r_f; st.S_t = S_t;
+        st.c = c; st.R_t = R_t; st.R_d = B2 ? 0.0f : R_d; st.r = r_f; st.S_t = S_t;
         st.status = status; st.greedy = greedy ? 1 : 0; st.pad = 0;
         P.ws_stat[ui] = st;
+        if constexpr (B2) {   // the second chain's bonus row, as its own unit would write it
+          const size_t ui2 = (size_t)(b + 1) * (k + 1) + ipos;
+          UnitStat s2;
+          s2.c = c2; s2.R_t = R_d; s2.R_d = 0.0f; s2.r = 0.0f; s2.S_t = S_d;
+          s2.status = status_d; s2.greedy = greedy2 ? 1 : 0; s2.pad = 0;
+          P.ws_stat[ui2] = s2;
+          if (greedy2 && status_d == 0) P.ws_y[ui2] = A_d;
+        }
         if (status != 0 || greedy) {
           if (!P.tv_only && status == 0) {
             P.ws_y[ui] = A_t;
@@ -958,6 +1126,10 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
             }
           }
           if (LAZY && PAIR && status != 0) P.ws_acc[pi] = 0;   // an invalid position stops the chain
+          if (PAIR && status != 0) {   // no probabilities at an invalid position
+            if (P.out_p) P.out_p[pi] = __int_as_float(0x7fc00000);
+            if (P.out_q) P.out_q[pi] = __int_as_float(0x7fc00000);
+          }
           if (PAIR && P.out_tv) P.out_tv[pi] = status == 0 ? (A_t != A_d ? 1.0f : 0.0f) : __int_as_float(0x7fc00000);
         } else if (LAZY && PAIR) {
           P.ws_acc[pi] = m.cont;
@@ -968,6 +1140,19 @@ __device__ __forceinline__ int process_unit(const KParams& P, Small& S, const ui
     merged_wait();
   }
   const Merged M = mg;
+  if constexpr (B2) {   // each sampling row's per-range target mass, as for a lone bonus row
+    const int it = (int)g.rank() * NWARP + warp;
+    if (M.status == 0 && !greedy) {
+      const float pmass = mine.s_t * pow2_diff(mine.ref_t, M.IR_t);
+      if (lane == 0) { P.ws_p[ui * ITEMS_MAX + it] = pmass; P.ws_w[ui * ITEMS_MAX + it] = pmass; }
+    }
+    if (M.status_d == 0 && !greedy2) {
+      const size_t ui2 = (size_t)(b + 1) * (k + 1) + ipos;
+      const float pmass = mine.s_d * pow2_diff(mine.ref_d, M.IR_d);
+      if (lane == 0) { P.ws_p[ui2 * ITEMS_MAX + it] = pmass; P.ws_w[ui2 * ITEMS_MAX + it] = pmass; }
+    }
+    return 0;
+  }
   // cluster-uniform; an accepted position of a lazy walk needs no residual
   if (M.status != 0 || greedy || (LAZY && M.cont)) {
     if (!LAZY && own_x && tid == 0) cp_async_wait_all();   // no accept test: the copied uniform is not used
@@ -1098,7 +1283,9 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
   const unsigned cid = cl_id(), ncl = cl_count();
   const int k = P.k;
   const unsigned B = (unsigned)P.B;
-  const unsigned n_units = B * (unsigned)P.units_per_chain;   // below 2^31 (checked on the host)
+  // the verified positions, then the bonus rows (verification only), paired where the instance pairs them
+  constexpr bool PB = pairs_bonus_rows<R>();
+  const unsigned n_units = B * (unsigned)k + (P.units_per_chain > k ? (PB ? (B + 1u) >> 1 : B) : 0u);   // below 2^31
   const uint32_t bar = saddr(&S.bar);
   const uint4* blk_t = reinterpret_cast<const uint4*>(stage) + (size_t)(0 * NWARP + warp) * R * 32;
   const uint4* blk_d = reinterpret_cast<const uint4*>(stage) + (size_t)(1 * NWARP + warp) * R * 32;
@@ -1162,10 +1349,10 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
       const bool carry = refill;
       int cont;
       if (cur.ipos < k)
-        cont = process_unit<Tl, R, true, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
+        cont = process_unit<Tl, R, U_PAIR, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
                                                      P.tma && has_next, T, x, carry, tm);
       else
-        cont = process_unit<Tl, R, false, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
+        cont = process_unit<Tl, R, U_BONUS, ENT, true>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, nxt,
                                                       P.tma && has_next, T, x, carry, tm);
       phase ^= 1u;
       if (carry) {   // this unit's exchange brought the new reserve
@@ -1185,22 +1372,25 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_fused_kernel(const KPa
     }
   } else {
     unsigned u = cid;
-    Unit cur = unit_of(u, B);
-    if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
+    Unit cur = unit_of<PB>(u, B, (unsigned)k);
+    if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R, PB>(P, g, cur, bar, stage);
     PendingMass pm;
     pm.on = false;
     for (; u < n_units; u += ncl, phase ^= 1u) {
       const bool has_next = u + ncl < n_units;
-      const Unit next = unit_of(u + ncl, B);
+      const Unit next = unit_of<PB>(u + ncl, B, (unsigned)k);
       const float T = P.temperature[cur.b];
       const int x = cur.ipos < k && !P.tv_only ? P.tokens[(size_t)cur.b * k + cur.ipos] : 0;
       const bool tma_next = P.tma && has_next;
       if (cur.ipos < k)
-        process_unit<Tl, R, true, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
-                                              false, tm, &pm);
+        process_unit<Tl, R, U_PAIR, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T,
+                                                x, false, tm, &pm);
+      else if (PB && cur.b + 1 < (int)B)
+        process_unit<Tl, R, U_BONUS2, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next,
+                                                  T, 0, false, tm, &pm, P.temperature[cur.b + 1]);
       else
-        process_unit<Tl, R, false, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T, x,
-                                               false, tm, &pm);
+        process_unit<Tl, R, U_BONUS, ENT, false>(P, S, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, tma_next, T,
+                                                 x, false, tm, &pm);
       cur = next;
     }
     flush_mass(P, &pm);
@@ -1777,13 +1967,13 @@ __global__ void __launch_bounds__(NT, R <= 10 ? 2 : 1) sv_grad_kernel(const KPar
   __syncthreads();
   cluster_sync_all();
   unsigned u = cid;
-  Unit cur = unit_of(u, B);
+  Unit cur = pos_unit_of(u, B);
   if (P.tma && warp == 0 && u < n_units) issue_unit_load<Tl, R>(P, g, cur, bar, stage);
   unsigned phase = 0;
   int n1 = 0;
   for (; u < n_units; u += ncl, phase ^= 1u) {
     const bool has_next = u + ncl < n_units;
-    const Unit next = unit_of(u + ncl, B);
+    const Unit next = pos_unit_of(u + ncl, B);
     grad_unit<Tl, R>(P, S, gs, blk_t, blk_d, g, cur, phase, n1, bar, stage, next, P.tma && has_next,
                      P.temperature[cur.b]);
     cur = next;
@@ -2002,6 +2192,10 @@ static void free_ctx(spec_verify_ctx* h) {
   }
   free(h);
 }
+
+// Units of one verification call: the k verified positions of every chain,
+// then the bonus rows two to a unit.
+static long long verify_units(int batch, int k) { return (long long)batch * k + (batch + 1) / 2; }
 
 static int launch_fused(spec_verify_ctx* h, const KParams& P, long long units, cudaStream_t s, bool grad = false,
                         bool lazy = false) {
@@ -2313,7 +2507,7 @@ static int verify_impl(spec_verify_t h, int batch, const void* target_logits, co
   P.units_per_chain = h->k + 1; P.tv_only = 0;
   P.vec16 = h->tma_ok && al16(target_logits) && al16(draft_logits);
   P.tma = bulk_ok && P.vec16;
-  int rc = launch_fused(h, P, (long long)batch * (h->k + 1), s);
+  int rc = launch_fused(h, P, verify_units(batch, h->k), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(h, P, draft_tokens, out_tokens, out_tau, s);
 }
@@ -2406,7 +2600,7 @@ int spec_verify_noalloc(int batch, int k, int vocab, int logit_dtype, const void
   P.units_per_chain = k + 1; P.tv_only = 0;
   P.tma = h.tma_ok && al16(target_logits) && al16(draft_logits);
   P.vec16 = P.tma;
-  int rc = launch_fused(&h, P, (long long)batch * (k + 1), s);
+  int rc = launch_fused(&h, P, verify_units(batch, k), s);
   if (rc != SV_OK) return rc;
   return launch_finalize(&h, P, draft_tokens, out_tokens, out_tau, s);
 }

@@ -97,3 +97,15 @@ def test_entropy_special_rows(lib, oracle):
     assert np.all(np.isnan(ex["entropy_target"][1])) and np.isnan(ex["entropy_target"][2, 1])
     assert not np.isnan(ex["entropy_target"][2, 0]) and np.isnan(ex["entropy_draft"][3, 0])
     assert abs(float(ex["entropy_draft"][5, 1]) - np.log(4096)) <= ATOL + RTOL * np.log(4096)
+
+
+def test_entropy_bonus_pairs(lib, oracle):
+    """Bonus rows two chains to a unit, each at its own temperature (greedy next
+    to sampling, two temperatures, an invalid one, the odd last chain alone)."""
+    temps = [0.0, 1.0, 0.7, 0.0, 1.3, 0.5, -1.0, 0.9, 0.0]
+    w = si.Workload("ent_bonus_pairs", len(temps), 2, 32001, si.BF16, 2.0, draft_sigma=0.8)
+    b = si.generate(w)
+    b.temperature[:] = temps
+    ex, want_t, want_d = check(lib, oracle, w, b)
+    assert ex["entropy_target"][0, w.k] == 0.0 and ex["entropy_target"][3, w.k] == 0.0
+    assert np.isnan(ex["entropy_target"][6, w.k]) and not np.isnan(ex["entropy_target"][7, w.k])

@@ -132,6 +132,27 @@ def test_invalid_chains_flagged(lib, oracle):
     assert list(np.nonzero(got["tau"] < 0)[0]) == [1, 2, 3, 4, 5, 6]
 
 
+# The bonus rows of chains 2j and 2j + 1 share one unit; each row keeps its own
+# chain's temperature and status.  Pairs here: greedy next to sampling (both
+# orders), two greedy, two temperatures, an invalid temperature next to a NaN
+# bonus row, a fully masked bonus row next to a valid one, and the odd last
+# chain alone.
+BONUS_TEMPS = [0.0, 1.0, 0.7, 0.0, 0.0, 0.0, 1.3, 0.5, -1.0, 0.9, 0.8, 1.1, 0.6]
+
+
+@pytest.mark.parametrize("V,dtype", [(5000, si.FP32), (151552, si.BF16)])
+def test_bonus_pairs_mixed_chains(lib, oracle, V, dtype):
+    w = si.Workload(f"bonus_pairs_V{V}", len(BONUS_TEMPS), 3, V, dtype, 2.0, draft_sigma=0.6)
+    b = si.generate(w)
+    b.temperature[:] = BONUS_TEMPS
+    nan = np.uint16(0x7FC0) if dtype == si.BF16 else np.float32(np.nan)
+    neg_inf = np.uint16(0xFF80) if dtype == si.BF16 else np.float32(-np.inf)
+    b.target[9, w.k, 17] = nan
+    b.target[11, w.k, :] = neg_inf
+    got, ref, _ = check(lib, oracle, w, b)
+    assert list(np.nonzero(got["tau"] < 0)[0]) == [8, 9, 11]
+
+
 def test_spec_verify_tv(lib, oracle):
     w = si.C5.scaled(batch=24)
     b = si.generate(w)
